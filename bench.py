@@ -1,0 +1,369 @@
+"""Benchmark: batched speculative-decoding verification on GB300.
+
+One step = one spec_verify call (setup, row pass, finalize) over the
+B=256, k=15, V=151936 bfloat16 batch with top-k 50 / top-p 0.9 on both
+distributions (2.41 GB of logits, far larger than the 129 MB L2, so no flush is
+needed between steps).  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Metric: verified rows per second (a verified row is one (request, position)
+pair, sum_b (k_b + 1) per call), whole job over all ranks.  The roofline object
+reports the row-pass kernel's achieved HBM bandwidth from the algorithmic bytes
+(every target and draft logit once) over its CUDA-event duration.
+
+--impl reference times the CPU oracle (the plain double-precision statement of
+the method) on the host cores, on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank verifies its own independently seeded batch
+(weak scaling, no data-path collective); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import signal
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "spec-verify rows/s and HBM GB/s vs ~8 TB/s peak at B=256,k=15,V=151936 bf16"
+UNIT = "rows/s"
+WORKLOAD = "B=256 k=15 V=151936 bf16 logits, temperature 1, top-k 50 + top-p 0.9 on p and q"
+L2_NOTE = "inputs larger than L2 (2.41 GB of logits vs 129 MB), no flush"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rowpass_c4_traffic.json")
+KERNEL_SOURCES = ["sv_internal.cuh", "sv_select.cuh", "sv_rowpass.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c4")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_13_gb300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy read+write)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (profiling recipe, 6.8 TB/s)"
+
+
+def recorded_traffic(bytes_per_launch):
+    """DRAM bytes per row-pass launch from the committed ncu summary, only if
+    it was taken on the current kernel source."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)],
+                stdout=self.file, stderr=subprocess.DEVNULL, start_new_session=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            try:
+                os.killpg(self.proc.pid, signal.SIGTERM)
+            except Exception:
+                pass
+            self.proc.wait(timeout=10)
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(",") for l in self.file.read().splitlines() if l.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(batch_gpu, budget_s=12.0):
+    """Oracle on the host cores over a bounded sample of the workload's
+    requests (per-request parallel over all cores)."""
+    import torch
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    B = batch_gpu.batch
+    # calibrate on a small slice, then size the sample for ~budget_s of wall time
+    n0 = min(B, max(cores, 8))
+    sub = batch_gpu.requests(range(n0)).to("cpu")
+    t0 = time.perf_counter()
+    oracle.verify(sub.target, sub.draft, sub.draft_tokens, sub.k_per_req, sub.temperature,
+                  sub.top_k, sub.top_p, sub.uniforms, threads=cores)
+    dt = time.perf_counter() - t0
+    n = int(min(B, max(n0, n0 * budget_s / max(dt, 1e-3))))
+    sub = batch_gpu.requests(range(n)).to("cpu")
+    t0 = time.perf_counter()
+    oracle.verify(sub.target, sub.draft, sub.draft_tokens, sub.k_per_req, sub.temperature,
+                  sub.top_k, sub.top_p, sub.uniforms, threads=cores)
+    dt = time.perf_counter() - t0
+    rows = sub.target_rows
+    del sub
+    torch.cuda.empty_cache()
+    return {"value": rows / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {B} requests ({rows} verified rows), per-request "
+                      f"parallel over {cores} host threads, {dt:.2f} s wall"}
+
+
+def run_reference(args, ws, rank):
+    """The reference arm: the oracle as it stands, timed on the host cores."""
+    if rank != 0:
+        return
+    import torch
+    import oracle
+    from speculative_decoding_verification_13_gb300 import workloads
+    oracle.build()
+    cores = os.cpu_count() or 1
+    B = workloads.CONFIGS[args.config]["B"]
+    gen = "cuda" if torch.cuda.is_available() else "cpu"
+    full = workloads.make_batch(args.config, device=gen, batch=min(B, cores))
+    # a bounded sample per step: one request per host thread, shrunk to a
+    # single request when K + W steps would otherwise exceed ~150 s
+    n = min(B, cores)
+    sub = full.requests(range(n)).to("cpu")
+    run = lambda: oracle.verify(sub.target, sub.draft, sub.draft_tokens, sub.k_per_req,
+                                sub.temperature, sub.top_k, sub.top_p, sub.uniforms,
+                                threads=cores)
+    t0 = time.perf_counter()
+    run()
+    if (time.perf_counter() - t0) * (args.steps + args.warmup) > 150.0 and n > 1:
+        n = 1
+        sub = full.requests(range(n)).to("cpu")
+    del full
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = sub.target_rows / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded Zipf-plus-Gaussian logits, see workloads.py)",
+        "config": {"workload": WORKLOAD, "sample_requests": n, "global_batch": B},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} requests ({sub.target_rows} verified rows) of the same "
+                                   f"workload per step, per-request parallel over {cores} "
+                                   f"threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    import torch
+    import speculative_decoding_verification_13_gb300 as sv
+    from speculative_decoding_verification_13_gb300 import build as cuda_build
+    from speculative_decoding_verification_13_gb300 import workloads
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0:
+        cuda_build.build()
+    if pg:
+        pg.barrier()
+    sv.load_library()
+
+    batch = workloads.make_batch(args.config, device=dev, seed_offset=rank)
+    B, Rt, Rd, V = batch.batch, batch.target_rows, batch.draft_rows, batch.vocab
+    bytes_per_step = batch.logit_bytes()
+    v = sv.Verifier(dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    tok = torch.empty(Rt, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda evs=None: v(batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
+                              batch.temperature, batch.uniforms, batch.top_k, batch.top_p,
+                              out_accept_len=acc, out_tokens=tok, rowpass_events=evs)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    code = v.error()[0]
+    if code != 0:
+        raise RuntimeError(f"device data error {code} during warm-up")
+
+    # timed region: K steps, row-pass events per step
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        call(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    step_ms = start.elapsed_time(end) / args.steps
+    rowpass_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    clk = clocks.stop() if clocks else None
+
+    if pg:
+        t = torch.tensor([step_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        step_ms = float(t.item())
+
+    # end to end through the public API from pinned host buffers
+    host = {k: getattr(batch, k).to("cpu").pin_memory() for k in
+            ("target", "draft", "draft_tokens", "k_per_req", "temperature", "top_k", "top_p",
+             "uniforms")}
+    dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    tok_h = torch.empty(Rt, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
+
+    def e2e_step():
+        for k_, t in host.items():
+            dbuf[k_].copy_(t, non_blocking=True)
+        a, o = v(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["k_per_req"],
+                 dbuf["temperature"], dbuf["uniforms"], dbuf["top_k"], dbuf["top_p"],
+                 out_accept_len=acc, out_tokens=tok)
+        acc_h.copy_(a, non_blocking=True)
+        tok_h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    del dbuf, host
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peak, peak_src = measured_peak()
+    achieved = bytes_per_step / (rowpass_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(bytes_per_step)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(batch)
+    line = {
+        "metric": METRIC,
+        "value": ws * Rt / (step_ms * 1e-3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Zipf-plus-Gaussian logits, see workloads.py)",
+        "config": {"workload": WORKLOAD, "global_batch": ws * B, "per_gpu_batch": B,
+                   "k": 15, "vocab": V, "verified_rows_per_step": Rt,
+                   "logit_rows_per_step": Rt + Rd, "logit_bytes_per_step": bytes_per_step,
+                   "l2": L2_NOTE, "parallelism": f"replicas x{ws} (independent batches)"},
+        "hbm_gbs": bytes_per_step / (step_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "rowpass_kernel<bf16>", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": peak_src,
+                     "bytes_per_launch": bytes_per_step, "launch_ms": rowpass_ms},
+        "e2e": {"value": ws * Rt / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * specverify.h -- C ABI of the GB300 (sm_103a) batched speculative-decoding
+ * verification library (libspecverify.so).
+ *
+ * What one call computes.  A batch holds B requests.  Request b drafted k_b
+ * tokens x_0..x_{k_b-1} (0 <= k_b <= 32).  The target model supplied logits at
+ * k_b + 1 positions (after 0, 1, .., k_b drafted tokens: "Speculative decoding
+ * and multi-token prediction", section "Draft and verify", step Two; "DFlash"
+ * §4 step 4, p_1..p_{gamma+1}) and the drafter supplied logits at k_b
+ * positions.  Each row is turned into a temperature-scaled softmax ("FlashMap:
+ * Flow Map Speculative Decoding…" §5, draft_block step 5), optionally
+ * filtered by top-k and top-p, applied identically to target and draft rows
+ * ("Speculative decoding and multi-token prediction", "Why the output is
+ * identical").  Then:
+ *   - temperature 0 (greedy): the longest prefix of drafts equal to the target
+ *     argmax (lowest index on ties) is accepted and the target's own argmax
+ *     token is emitted at the first disagreement, or as the bonus token after
+ *     a full acceptance ("DFlash" §4 step 5; "Speculative decoding…",
+ *     "Draft and verify", step Three);
+ *   - temperature > 0 (sampling): draft i is accepted iff u_i < p_i(x_i) /
+ *     q_i(x_i) and verification stops at the first rejection ("FlashMap…" §4
+ *     "The Rejection Sampling Invariant", steps 1-2).  After a rejection at
+ *     position L one token is drawn from the normalised residual
+ *     max(0, p_L - q_L) ("FlashMap…" §4 step 3; "DFlash" §4); after a full
+ *     acceptance a bonus token is drawn from p_k.  Both draws use the
+ *     uniform u_k by inverse CDF in vocabulary-index order:
+ *     y* = min{ y : C_y > u_k * S }.
+ *
+ * Row layout.  Request b owns target rows t_off[b] .. t_off[b] + k_b with
+ * t_off[b] = sum_{j<b} (k_j + 1), and draft rows d_off[b] .. d_off[b] + k_b - 1
+ * with d_off[b] = t_off[b] - b (ragged batches are packed contiguously).
+ * draft_tokens[d_off[b] + i] is x_i; uniforms[t_off[b] + i] is u_i for i < k_b
+ * and uniforms[t_off[b] + k_b] drives the final draw; out_tokens uses the
+ * target-row layout: out_tokens[t_off[b] + j] is the j-th emitted token of
+ * request b, -1 after the last emitted one.  For a fixed k this is exactly a
+ * [B, k+1] matrix.
+ *
+ * Ownership and synchronisation.  Every pointer handed to spec_verify is a
+ * device pointer owned by the caller, including the workspace.  The library
+ * allocates nothing, frees nothing and never synchronises inside spec_verify:
+ * all work is enqueued on the caller's stream (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream) and results are visible in stream order.
+ * Concurrent calls are safe when they use distinct workspaces.
+ *
+ * Errors.  Argument errors that the host can see (null pointers, bad sizes,
+ * misalignment, unsupported dtype, workspace too small) return a nonzero
+ * SV_ERR_* code before anything is enqueued.  Data errors live in device
+ * memory and are found by the kernels: the first one is recorded in the
+ * workspace (read it with spec_verify_get_error) and every affected request
+ * gets out_accept_len = -1 and out_tokens = -1.  Kernels never trap.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define SV_OK 0
+#define SV_ERR_ARG 1          /* null pointer, negative or inconsistent size   */
+#define SV_ERR_UNSUPPORTED 2  /* dtype, vocabulary size, alignment, stride    */
+#define SV_ERR_CUDA 3         /* a CUDA runtime call or launch failed          */
+#define SV_ERR_WORKSPACE 4    /* workspace missing, too small or misaligned    */
+/* data errors, found on the device (one request each unless stated) */
+#define SV_ERR_DATA_K 16            /* k_b outside [0, SV_MAX_K]                 */
+#define SV_ERR_DATA_TEMPERATURE 17  /* temperature negative, NaN or infinite     */
+#define SV_ERR_DATA_TOP_P 18        /* top_p outside (0, 1]                      */
+#define SV_ERR_DATA_TOP_K 19        /* top_k < 0, 0 < top_k < V with top_k >     */
+                                    /* SV_TOPK_MAX, or top-p without top-k        */
+#define SV_ERR_DATA_TOKEN 20        /* a draft token outside [0, V)              */
+#define SV_ERR_DATA_ROWS 21         /* sum(k+1) != target rows or sum(k) !=      */
+                                    /* draft rows (whole batch)                  */
+#define SV_ERR_DATA_LOGIT 22        /* NaN or +inf logit, or (sampling) a row    */
+                                    /* with no finite logit                      */
+#define SV_ERR_DATA_NO_DRAFT 23     /* temperature > 0 but draft logits absent   */
+#define SV_ERR_TIMEOUT 24           /* an internal bounded wait expired          */
+#define SV_ERR_INTERNAL 25          /* an internal capacity invariant failed     */
+
+/* ---- limits -------------------------------------------------------------- */
+#define SV_MAX_K 32              /* drafts per request (one warp ballot)       */
+#define SV_TOPK_MAX 256          /* largest active top-k                       */
+#define SV_VOCAB_MAX (1 << 22)   /* largest vocabulary                         */
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* A [rows, vocab] logit matrix in device memory.  `data` must be 16-byte
+ * aligned and row_stride * element_size must be a multiple of 16 bytes
+ * (row_stride >= vocab, in elements).  Target and draft share one dtype. */
+typedef struct {
+  const void* data;
+  int32_t dtype;      /* sv_dtype */
+  int32_t vocab;      /* V, 1 <= V <= SV_VOCAB_MAX */
+  int64_t rows;
+  int64_t row_stride; /* elements */
+} sv_logits;
+
+/* Optional extras of spec_verify; pass NULL for none. */
+typedef struct {
+  /* [draft_rows, 2] device doubles: (p_i(x_i), q_i(x_i)) of every sampled
+   * request, NaN for greedy and failed requests (parity / diagnostics). */
+  double* out_pq;
+  /* cudaEvent_t handles recorded on the stream right before and right after
+   * the row-streaming kernel (profiling); NULL to skip. */
+  void* event_rowpass_begin;
+  void* event_rowpass_end;
+} sv_options;
+
+/* Bytes of device workspace spec_verify needs for this shape; 0 on bad
+ * arguments.  The workspace must be 256-byte aligned and must not be used by
+ * two calls that can run concurrently. */
+size_t spec_verify_workspace_size(int32_t batch, int64_t target_rows, int64_t draft_rows);
+
+/* Batched verification (see the file comment for what it computes).
+ *   target_logits  [R_t, V]  R_t = sum_b (k_b + 1)
+ *   draft_logits   [R_d, V]  R_d = sum_b k_b; the descriptor is required, its
+ *                  `data` may be NULL when every temperature is 0
+ *   draft_tokens   [R_d] int32            k_per_req   [B] int32, 0..SV_MAX_K
+ *   temperature    [B] float, 0 = greedy
+ *   top_k          [B] int32 or NULL; 0 or >= V switches top-k off
+ *   top_p          [B] float or NULL; 1 switches top-p off; (0, 1]
+ *   uniforms       [R_t] float in [0, 1)
+ *   out_accept_len [B] int32 (L, or -1 on a data error)
+ *   out_tokens     [R_t] int32
+ *   stream         cudaStream_t
+ *   batch          B >= 0
+ *   workspace      >= spec_verify_workspace_size(B, R_t, R_d) bytes
+ * Returns SV_OK once the work is enqueued, else an SV_ERR_* code. */
+int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
+                const int32_t* draft_tokens, const int32_t* k_per_req,
+                const float* temperature, const int32_t* top_k, const float* top_p,
+                const float* uniforms, int32_t* out_accept_len, int32_t* out_tokens,
+                void* stream, int32_t batch, void* workspace, size_t workspace_bytes,
+                const sv_options* options);
+
+/* Synchronises `stream`, then reads the first data error recorded by the last
+ * call that used `workspace`: *code (SV_OK if none), *request and *row (-1
+ * when not applicable).  Test / debug use. */
+int spec_verify_get_error(const void* workspace, void* stream, int32_t* code,
+                          int32_t* request, int64_t* row);
+
+/* Synchronises `stream` and copies the per-row intermediate results of the
+ * last call into host buffers (test / debug use).  Rows are numbered target
+ * rows first (0 .. R_t-1), then draft rows (R_t .. R_t+R_d-1).
+ *   stats      [R, 4] doubles: row max logit, softmax normaliser (sampling rows:
+ *              sum of exp((x - max)/T) for unfiltered rows, 0 for filtered),
+ *              p(x) of the row's draft token (NaN if none), greedy argmax
+ *              (-1 if not computed)
+ *   kept_count [R] int32: size of the kept set after top-k / top-p (0 if the
+ *              row was not filtered)
+ *   kept_idx   [R, SV_TOPK_MAX] int32 and kept_p [R, SV_TOPK_MAX] doubles:
+ *              the kept tokens in (logit desc, index asc) order and their
+ *              renormalised probabilities.
+ * Any output pointer may be NULL. */
+int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t batch,
+                          int64_t target_rows, int64_t draft_rows, void* stream,
+                          double* stats, int32_t* kept_count, int32_t* kept_idx,
+                          double* kept_p);
+
+/* Human-readable text of a status code. */
+const char* spec_verify_strerror(int code);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,255 @@
+"""GB300-native batched speculative-decoding verification.
+
+Python binding of ``libspecverify.so`` (C ABI declared in
+``include/specverify.h``).  This module only marshals arguments: every step of
+verification runs in the library's sm_103a kernels.  PyTorch supplies device
+memory and streams.  There is no CPU fallback: if the library has not been
+built, importing the binding's entry points raises.
+
+Typical use::
+
+    import speculative_decoding_verification_13_gb300 as sv
+    accept_len, tokens = sv.verify(target, draft, draft_tokens, k_per_req,
+                                   temperature, uniforms, top_k=top_k, top_p=top_p)
+
+Row layout (see the header): request b owns target rows t_off[b]..t_off[b]+k_b
+(t_off[b] = sum_{j<b}(k_j+1)) and draft rows t_off[b]-b..; ``uniforms`` and the
+returned ``tokens`` use the target-row layout.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
+           "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
+
+SV_OK = 0
+SV_F32, SV_BF16 = 0, 1
+SV_MAX_K = 32
+SV_TOPK_MAX = 256
+SV_VOCAB_MAX = 1 << 22
+
+ERROR_NAMES = {
+    0: "SV_OK", 1: "SV_ERR_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
+    4: "SV_ERR_WORKSPACE", 16: "SV_ERR_DATA_K", 17: "SV_ERR_DATA_TEMPERATURE",
+    18: "SV_ERR_DATA_TOP_P", 19: "SV_ERR_DATA_TOP_K", 20: "SV_ERR_DATA_TOKEN",
+    21: "SV_ERR_DATA_ROWS", 22: "SV_ERR_DATA_LOGIT", 23: "SV_ERR_DATA_NO_DRAFT",
+    24: "SV_ERR_TIMEOUT", 25: "SV_ERR_INTERNAL",
+}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}{': ' if what else ''}{ERROR_NAMES.get(code, code)} "
+                         f"({strerror(code)})")
+
+
+class _Logits(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                ("vocab", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("row_stride", ctypes.c_int64)]
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("out_pq", ctypes.c_void_p), ("event_rowpass_begin", ctypes.c_void_p),
+                ("event_rowpass_end", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libspecverify.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` "
+                    "(the CUDA library is required; there is no fallback)")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+            lib.spec_verify_workspace_size.restype = sz
+            lib.spec_verify_workspace_size.argtypes = [i32, i64, i64]
+            lib.spec_verify.restype = ctypes.c_int
+            lib.spec_verify.argtypes = [ctypes.POINTER(_Logits), ctypes.POINTER(_Logits),
+                                        P, P, P, P, P, P, P, P, P, i32, P, sz,
+                                        ctypes.POINTER(_Options)]
+            lib.spec_verify_get_error.restype = ctypes.c_int
+            lib.spec_verify_get_error.argtypes = [P, P, P, P, P]
+            lib.spec_verify_dump_rows.restype = ctypes.c_int
+            lib.spec_verify_dump_rows.argtypes = [P, sz, i32, i64, i64, P, P, P, P, P]
+            lib.spec_verify_strerror.restype = ctypes.c_char_p
+            lib.spec_verify_strerror.argtypes = [ctypes.c_int]
+            lib.spec_verify_version.restype = ctypes.c_int
+            lib.spec_verify_version.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load_library().spec_verify_strerror(int(code)).decode()
+
+
+def workspace_size(batch: int, target_rows: int, draft_rows: int) -> int:
+    return int(load_library().spec_verify_workspace_size(int(batch), int(target_rows),
+                                                         int(draft_rows)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(t, name, dtype, ndim=1):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimension(s)")
+    if ndim == 1 and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _logits_desc(x, V=None):
+    if x is None:
+        return _Logits(None, SV_BF16, V or 0, 0, V or 0)
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 2:
+        raise TypeError("logits must be 2-D CUDA tensors")
+    if x.dtype == torch.bfloat16:
+        dt = SV_BF16
+    elif x.dtype == torch.float32:
+        dt = SV_F32
+    else:
+        raise TypeError(f"logits must be float32 or bfloat16, got {x.dtype}")
+    if x.stride(1) != 1:
+        raise ValueError("logit rows must be contiguous")
+    rows, V = x.shape
+    stride = x.stride(0) if rows > 1 else V
+    return _Logits(x.data_ptr() if x.numel() else None, dt, V, rows, stride)
+
+
+class Verifier:
+    """Reusable caller-side state: a workspace sized for the largest batch seen
+    and the output buffers.  One Verifier per stream (workspaces must not be
+    shared by calls that can overlap)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.workspace = None
+
+    def _workspace(self, B, Rt, Rd):
+        need = workspace_size(B, Rt, Rd)
+        if need == 0 and (B or Rt or Rd):
+            raise SpecVerifyError(1, "workspace_size")
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self.workspace
+
+    def __call__(self, target, draft, draft_tokens, k_per_req, temperature, uniforms,
+                 top_k=None, top_p=None, *, out_accept_len=None, out_tokens=None,
+                 out_pq=None, stream=None, rowpass_events=None):
+        lib = load_library()
+        B = int(k_per_req.shape[0])
+        _check(k_per_req, "k_per_req", torch.int32)
+        _check(temperature, "temperature", torch.float32)
+        _check(uniforms, "uniforms", torch.float32)
+        _check(draft_tokens, "draft_tokens", torch.int32)
+        _check(top_k, "top_k", torch.int32)
+        _check(top_p, "top_p", torch.float32)
+        td = _logits_desc(target)
+        dd = _logits_desc(draft, td.vocab)
+        if draft is None:
+            dd.rows = td.rows - B
+            dd.dtype = td.dtype
+        Rt, Rd = int(td.rows), int(dd.rows)
+        if out_accept_len is None:
+            out_accept_len = torch.empty(B, dtype=torch.int32, device=target.device)
+        if out_tokens is None:
+            out_tokens = torch.empty(Rt, dtype=torch.int32, device=target.device)
+        _check(out_accept_len, "out_accept_len", torch.int32)
+        _check(out_tokens, "out_tokens", torch.int32)
+        ws = self._workspace(B, Rt, Rd)
+        opts = None
+        if out_pq is not None or rowpass_events is not None:
+            ev0, ev1 = rowpass_events if rowpass_events is not None else (None, None)
+            opts = _Options(_ptr(out_pq),
+                            ctypes.c_void_p(ev0.cuda_event) if ev0 is not None else None,
+                            ctypes.c_void_p(ev1.cuda_event) if ev1 is not None else None)
+        rc = lib.spec_verify(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
+                             _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                             _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
+                             _stream_handle(stream), B, _ptr(ws), ws.numel(),
+                             ctypes.byref(opts) if opts is not None else None)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify")
+        return out_accept_len, out_tokens
+
+    def error(self, stream=None):
+        return get_error(self.workspace, stream)
+
+    def dump(self, batch, target_rows, draft_rows, stream=None):
+        return dump_rows(self.workspace, batch, target_rows, draft_rows, stream)
+
+
+_default = {}
+
+
+def verify(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k=None,
+           top_p=None, **kw):
+    """One-shot verification with a per-device cached Verifier.  Returns
+    ``(accept_len [B] int32, tokens [R_t] int32)`` on the device."""
+    dev = target.device
+    v = _default.get(dev)
+    if v is None:
+        v = _default[dev] = Verifier(dev)
+    return v(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k, top_p, **kw)
+
+
+def get_error(workspace, stream=None):
+    """Synchronise and return ``(code, request, row)`` of the first data error."""
+    code, req, row = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int64()
+    rc = load_library().spec_verify_get_error(_ptr(workspace), _stream_handle(stream),
+                                              ctypes.byref(code), ctypes.byref(req),
+                                              ctypes.byref(row))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_get_error")
+    return code.value, req.value, row.value
+
+
+def dump_rows(workspace, batch, target_rows, draft_rows, stream=None):
+    """Per-row intermediate results of the last call (host tensors)."""
+    R = target_rows + draft_rows
+    stats = torch.empty(R, 4, dtype=torch.float64)
+    kept = torch.empty(R, dtype=torch.int32)
+    kidx = torch.empty(R, SV_TOPK_MAX, dtype=torch.int32)
+    kp = torch.empty(R, SV_TOPK_MAX, dtype=torch.float64)
+    rc = load_library().spec_verify_dump_rows(_ptr(workspace), workspace.numel(), batch,
+                                              target_rows, draft_rows, _stream_handle(stream),
+                                              _ptr(stats), _ptr(kept), _ptr(kidx), _ptr(kp))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_dump_rows")
+    return dict(stats=stats, kept_count=kept, kept_idx=kidx, kept_p=kp)

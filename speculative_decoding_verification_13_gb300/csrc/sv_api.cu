@@ -1,0 +1,202 @@
+// Host side of the C ABI: argument validation, workspace layout, and the
+// three launches (setup -> row pass -> finalize) on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "sv_internal.cuh"
+
+namespace sv {
+cudaError_t rowpass_configure();
+cudaError_t finalize_configure();
+}  // namespace sv
+
+using namespace sv;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  int sms = 0;
+  bool ready = false;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+// Per-device one-time set-up: SM count and the kernels' shared-memory limits.
+int prepare_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev[dev].ready) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return SV_ERR_CUDA;
+    if (rowpass_configure() != cudaSuccess || finalize_configure() != cudaSuccess)
+      return SV_ERR_CUDA;
+    g_dev[dev].sms = n;
+    g_dev[dev].ready = true;
+  }
+  *sms = g_dev[dev].sms;
+  return SV_OK;
+}
+
+bool misaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+size_t elem_size(int dtype) { return dtype == SV_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int32_t batch, int64_t target_rows, int64_t draft_rows) {
+  if (batch < 0 || target_rows < 0 || draft_rows < 0 || target_rows + draft_rows >= INT_MAX)
+    return 0;
+  return ws_layout(batch, target_rows, draft_rows).total;
+}
+
+int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
+                const int32_t* draft_tokens, const int32_t* k_per_req, const float* temperature,
+                const int32_t* top_k, const float* top_p, const float* uniforms,
+                int32_t* out_accept_len, int32_t* out_tokens, void* stream, int32_t batch,
+                void* workspace, size_t workspace_bytes, const sv_options* options) {
+  if (!target_logits || !draft_logits || batch < 0) return SV_ERR_ARG;
+  const sv_logits& t = *target_logits;
+  const sv_logits& d = *draft_logits;
+  if (t.dtype != SV_F32 && t.dtype != SV_BF16) return SV_ERR_UNSUPPORTED;
+  if (d.dtype != t.dtype) return SV_ERR_UNSUPPORTED;
+  if (d.vocab != t.vocab || t.vocab < 1) return SV_ERR_ARG;
+  if (t.vocab > SV_VOCAB_MAX) return SV_ERR_UNSUPPORTED;
+  if (t.rows < 0 || d.rows < 0 || t.rows + d.rows >= INT_MAX) return SV_ERR_ARG;
+  // sum_b (k_b + 1) = B + sum_b k_b, whatever the k_b are
+  if (t.rows != int64_t(batch) + d.rows) return SV_ERR_ARG;
+  const size_t es = elem_size(t.dtype);
+  if (t.row_stride < t.vocab) return SV_ERR_ARG;
+  if (d.data && d.rows > 0 && d.row_stride < d.vocab) return SV_ERR_ARG;
+  if (batch > 0 && (!t.data || !k_per_req || !temperature || !uniforms || !out_accept_len ||
+                    !out_tokens))
+    return SV_ERR_ARG;
+  if (d.rows > 0 && !draft_tokens) return SV_ERR_ARG;
+  if (misaligned(t.data, 16) || (size_t(t.row_stride) * es) % 16 != 0) return SV_ERR_UNSUPPORTED;
+  if (d.data && (misaligned(d.data, 16) || (size_t(d.row_stride) * es) % 16 != 0))
+    return SV_ERR_UNSUPPORTED;
+  const WsLayout L = ws_layout(batch, t.rows, d.rows);
+  if (!workspace || misaligned(workspace, 256) || workspace_bytes < L.total)
+    return SV_ERR_WORKSPACE;
+  if (batch == 0) return SV_OK;
+
+  int sms = 0;
+  if (int rc = prepare_device(&sms)) return rc;
+
+  Problem P;
+  P.target = t.data;
+  P.draft = d.data;
+  P.t_stride = t.row_stride;
+  P.d_stride = d.data ? d.row_stride : 0;
+  P.Rt = t.rows;
+  P.Rd = d.rows;
+  P.V = t.vocab;
+  P.B = batch;
+  P.draft_tokens = draft_tokens;
+  P.k_per_req = k_per_req;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.uniforms = uniforms;
+  P.out_accept_len = out_accept_len;
+  P.out_tokens = out_tokens;
+  P.out_pq = options ? options->out_pq : nullptr;
+  P.ws = ws_bind(workspace, L);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_setup(P, s) != cudaSuccess) return SV_ERR_CUDA;
+  const int64_t rows = t.rows + d.rows;
+  const int grid = int(rows < sms ? rows : sms);
+  if (options && options->event_rowpass_begin &&
+      cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (grid > 0 && launch_rowpass(P, t.dtype == SV_BF16, grid, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (options && options->event_rowpass_end &&
+      cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (launch_finalize(P, t.dtype == SV_BF16, s) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+int spec_verify_get_error(const void* workspace, void* stream, int32_t* code, int32_t* request,
+                          int64_t* row) {
+  if (!workspace || !code) return SV_ERR_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SV_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  *code = h.err_code;
+  if (request) *request = h.err_req;
+  if (row) *row = h.err_row;
+  return SV_OK;
+}
+
+int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t batch,
+                          int64_t target_rows, int64_t draft_rows, void* stream, double* stats,
+                          int32_t* kept_count, int32_t* kept_idx, double* kept_p) {
+  if (!workspace || batch < 0 || target_rows < 0 || draft_rows < 0) return SV_ERR_ARG;
+  const WsLayout L = ws_layout(batch, target_rows, draft_rows);
+  if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SV_ERR_CUDA;
+  const char* base = static_cast<const char*>(workspace);
+  const size_t R = size_t(target_rows + draft_rows);
+  if (R == 0) return SV_OK;
+  if (stats || kept_count) {
+    std::vector<RowStat> st(R);
+    if (cudaMemcpy(st.data(), base + L.off_stats, R * sizeof(RowStat), cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+      return SV_ERR_CUDA;
+    for (size_t r = 0; r < R; ++r) {
+      if (stats) {
+        stats[4 * r + 0] = st[r].m;
+        stats[4 * r + 1] = st[r].s;
+        stats[4 * r + 2] = st[r].pg;
+        stats[4 * r + 3] = st[r].arg;
+      }
+      if (kept_count) kept_count[r] = st[r].mode == kTopk ? st[r].kept : 0;
+    }
+  }
+  if (kept_idx && cudaMemcpy(kept_idx, base + L.off_cidx, R * kTopkMax * sizeof(int32_t),
+                             cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (kept_p && cudaMemcpy(kept_p, base + L.off_cp, R * kTopkMax * sizeof(double),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+const char* spec_verify_strerror(int code) {
+  switch (code) {
+    case SV_OK: return "ok";
+    case SV_ERR_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported dtype, vocabulary size, alignment or stride";
+    case SV_ERR_CUDA: return "CUDA runtime error";
+    case SV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SV_ERR_DATA_K: return "k_per_req outside [0, SV_MAX_K]";
+    case SV_ERR_DATA_TEMPERATURE: return "temperature negative, NaN or infinite";
+    case SV_ERR_DATA_TOP_P: return "top_p outside (0, 1]";
+    case SV_ERR_DATA_TOP_K: return "top_k negative, above SV_TOPK_MAX, or top-p without top-k";
+    case SV_ERR_DATA_TOKEN: return "draft token outside [0, V)";
+    case SV_ERR_DATA_ROWS: return "row counts do not match k_per_req";
+    case SV_ERR_DATA_LOGIT: return "NaN or +inf logit, or a sampled row without a finite logit";
+    case SV_ERR_DATA_NO_DRAFT: return "temperature > 0 without draft logits";
+    case SV_ERR_TIMEOUT: return "internal bounded wait expired";
+    case SV_ERR_INTERNAL: return "internal capacity invariant failed";
+    default: return "unknown status";
+  }
+}
+
+int spec_verify_version(void) { return 100; }
+
+}  // extern "C"

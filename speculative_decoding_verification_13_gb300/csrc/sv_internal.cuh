@@ -1,0 +1,243 @@
+// Internal declarations of libspecverify: workspace layout, kernel parameter
+// block and small device helpers (inline PTX for mbarriers, bulk copies and
+// named barriers).  Nothing here is shared with the oracle.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/specverify.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------- constants
+constexpr int kConsumerWarps = 16;                       // warps that read tiles
+constexpr int kConsumers = kConsumerWarps * 32;          // 512 threads
+constexpr int kRowpassThreads = kConsumers + 32;         // + one producer warp
+constexpr int kTileBytes = 16384;                        // one bulk copy
+constexpr int kStages = 8;                               // smem ring depth
+constexpr int kBufCap = 4096;                            // top-k candidate buffer
+constexpr int kScratch = 1024;                           // selection scratch entries
+constexpr int kTopkMax = SV_TOPK_MAX;
+constexpr int kFinalThreads = 256;
+constexpr int kFinalTileElems = kFinalThreads * 8;       // elements per scan tile
+constexpr int kMaxFinalTiles = (SV_VOCAB_MAX + kFinalTileElems - 1) / kFinalTileElems;
+constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
+
+// Row modes chosen per request by the setup kernel.
+enum RowMode : int { kSkip = 0, kStats = 1, kArgmax = 2, kTopk = 3 };
+
+// ---------------------------------------------------------------- workspace
+struct WsHeader {
+  int32_t err_code;
+  int32_t err_req;
+  int64_t err_row;
+  int32_t n_active;     // rows the row pass must stream
+  int32_t global_err;   // batch-level data error (row counts)
+  int32_t pad[10];
+};
+
+struct RowStat {
+  double s;     // softmax normaliser (unfiltered sampling rows)
+  double pg;    // p(x) of the row's draft token
+  float m;      // row max logit
+  int32_t arg;  // greedy argmax
+  int32_t kept; // kept-set size (filtered rows)
+  int32_t mode;
+};
+
+struct Ws {
+  WsHeader* hdr;
+  int32_t* t_off;    // [B + 1]
+  int32_t* req_flag; // [B]
+  int4* rowlist;     // [R] {row, request, gather token, (pos << 2) | mode}
+  RowStat* stats;    // [R]
+  int32_t* cand_idx; // [R, kTopkMax]
+  double* cand_p;    // [R, kTopkMax]
+};
+
+struct WsLayout {
+  size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
+  WsLayout L;
+  const int64_t R = Rt + Rd;
+  size_t o = align256(sizeof(WsHeader));
+  L.off_t_off = o;   o = align256(o + sizeof(int32_t) * (size_t)(B + 1));
+  L.off_flag = o;    o = align256(o + sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
+  L.off_rowlist = o; o = align256(o + sizeof(int4) * (size_t)(R > 0 ? R : 1));
+  L.off_stats = o;   o = align256(o + sizeof(RowStat) * (size_t)(R > 0 ? R : 1));
+  L.off_cidx = o;    o = align256(o + sizeof(int32_t) * kTopkMax * (size_t)(R > 0 ? R : 1));
+  L.off_cp = o;      o = align256(o + sizeof(double) * kTopkMax * (size_t)(R > 0 ? R : 1));
+  L.total = o;
+  return L;
+}
+
+inline Ws ws_bind(void* base, const WsLayout& L) {
+  char* p = static_cast<char*>(base);
+  Ws w;
+  w.hdr = reinterpret_cast<WsHeader*>(p);
+  w.t_off = reinterpret_cast<int32_t*>(p + L.off_t_off);
+  w.req_flag = reinterpret_cast<int32_t*>(p + L.off_flag);
+  w.rowlist = reinterpret_cast<int4*>(p + L.off_rowlist);
+  w.stats = reinterpret_cast<RowStat*>(p + L.off_stats);
+  w.cand_idx = reinterpret_cast<int32_t*>(p + L.off_cidx);
+  w.cand_p = reinterpret_cast<double*>(p + L.off_cp);
+  return w;
+}
+
+// Everything a kernel needs about one call.
+struct Problem {
+  const void* target;
+  const void* draft;
+  int64_t t_stride, d_stride;   // elements
+  int64_t Rt, Rd;
+  int32_t V;
+  int32_t B;
+  const int32_t* draft_tokens;
+  const int32_t* k_per_req;
+  const float* temperature;
+  const int32_t* top_k;         // may be null
+  const float* top_p;           // may be null
+  const float* uniforms;
+  int32_t* out_accept_len;
+  int32_t* out_tokens;
+  double* out_pq;               // may be null
+  Ws ws;
+};
+
+// ------------------------------------------------------- host-side launchers
+cudaError_t launch_setup(const Problem& P, cudaStream_t s);
+cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_finalize(const Problem& P, bool bf16, cudaStream_t s);
+size_t rowpass_smem_bytes();
+
+// ------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void record_error(WsHeader* h, int code, int req, int64_t row) {
+  if (atomicCAS(&h->err_code, 0, code) == 0) {
+    h->err_req = req;
+    h->err_row = row;
+  }
+}
+
+__device__ __forceinline__ void flag_request(const Ws& w, int b, int code, int64_t row) {
+  atomicCAS(&w.req_flag[b], 0, code);
+  record_error(w.hdr, code, b, row);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false when the limit ran out (the caller records SV_ERR_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// One bulk global -> shared copy completing on an mbarrier (TMA, non-tensor form).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Barrier among the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Total order used by top-k: (logit descending, index ascending).  The key is
+// the order-preserving unsigned image of the float (with -0 folded onto +0);
+// the low word holds ~index so that a smaller index compares larger.
+__device__ __forceinline__ uint64_t composite_key(float v, uint32_t idx) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  const uint32_t key = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~idx);
+}
+
+__device__ __forceinline__ float composite_value(uint64_t c) {
+  const uint32_t key = static_cast<uint32_t>(c >> 32);
+  const uint32_t b = (key & 0x80000000u) ? (key & 0x7fffffffu) : ~key;
+  return __uint_as_float(b);
+}
+
+__device__ __forceinline__ int32_t composite_index(uint64_t c) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(c));
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace sv

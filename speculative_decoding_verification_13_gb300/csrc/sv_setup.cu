@@ -1,0 +1,159 @@
+// Setup kernel: one CTA per call.  Computes the ragged row offsets
+// t_off[b] = sum_{j<b} (k_j + 1), validates every request's parameters and
+// drafted tokens, picks each row's mode and writes the list of rows the
+// streaming pass must read, ordered by request.
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kSetupThreads = 1024;
+
+// Exclusive scan over the CTA; *total receives the sum.
+__device__ int block_exclusive_scan(int v, int* total) {
+  __shared__ int s_warp[kSetupThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int y = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    s_warp[lane] = y;
+  }
+  __syncthreads();
+  const int excl = x - v + (warp ? s_warp[warp - 1] : 0);
+  *total = s_warp[kSetupThreads / 32 - 1];
+  __syncthreads();
+  return excl;
+}
+
+__global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
+  const Ws& w = P.ws;
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) {
+    w.hdr->err_code = 0;
+    w.hdr->err_req = -1;
+    w.hdr->err_row = -1;
+    w.hdr->n_active = 0;
+    w.hdr->global_err = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+
+  // Pass 1: row offsets; a k outside [0, SV_MAX_K] makes the layout undefined.
+  int carry = 0, carry_d = 0;
+  for (int base = 0; base < P.B; base += kSetupThreads) {
+    const int b = base + threadIdx.x;
+    int k = 0;
+    if (b < P.B) {
+      k = P.k_per_req[b];
+      if (k < 0 || k > SV_MAX_K) {
+        record_error(w.hdr, SV_ERR_DATA_K, b, -1);
+        atomicOr(&s_bad, 1);
+        k = 0;
+      }
+    }
+    int tot, totd;
+    const int ex = block_exclusive_scan(b < P.B ? k + 1 : 0, &tot);
+    block_exclusive_scan(b < P.B ? k : 0, &totd);
+    if (b < P.B) w.t_off[b] = carry + ex;
+    carry += tot;
+    carry_d += totd;
+  }
+  if (threadIdx.x == 0) {
+    w.t_off[P.B] = carry;
+    if (!s_bad && (carry != P.Rt || carry_d != P.Rd)) {
+      record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
+      s_bad = 1;
+    }
+    if (s_bad) w.hdr->global_err = 1;
+  }
+  __syncthreads();
+  if (s_bad) return;
+
+  // Pass 2: per-request validation, modes, and the active row list.
+  int carry_a = 0;
+  for (int base = 0; base < P.B; base += kSetupThreads) {
+    const int b = base + threadIdx.x;
+    int code = 0, active = 0, mode_t = kSkip, mode_d = kSkip, k = 0, t0 = 0, d0 = 0;
+    if (b < P.B) {
+      k = P.k_per_req[b];
+      t0 = w.t_off[b];
+      d0 = t0 - b;
+      const float T = P.temperature[b];
+      const float tp = P.top_p ? P.top_p[b] : 1.0f;
+      const int tk = P.top_k ? P.top_k[b] : 0;
+      const bool topk_on = tk > 0 && tk < P.V;
+      const bool filtered = T > 0.0f && (topk_on || tp < 1.0f);
+      if (!(T >= 0.0f) || isinf(T)) code = SV_ERR_DATA_TEMPERATURE;
+      else if (!(tp > 0.0f && tp <= 1.0f)) code = SV_ERR_DATA_TOP_P;
+      else if (tk < 0) code = SV_ERR_DATA_TOP_K;
+      else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
+      else if (T > 0.0f && k > 0 && P.draft == nullptr) code = SV_ERR_DATA_NO_DRAFT;
+      if (!code)
+        for (int i = 0; i < k; ++i) {
+          const int x = P.draft_tokens[d0 + i];
+          if (x < 0 || x >= P.V) {
+            code = SV_ERR_DATA_TOKEN;
+            break;
+          }
+        }
+      w.req_flag[b] = code;
+      if (code) {
+        record_error(w.hdr, code, b, -1);
+      } else if (T == 0.0f) {
+        mode_t = kArgmax;
+        active = k + 1;
+      } else {
+        mode_t = mode_d = filtered ? kTopk : kStats;
+        active = 2 * k + 1;
+      }
+    }
+    int tot;
+    const int a0 = carry_a + block_exclusive_scan(active, &tot);
+    carry_a += tot;
+    if (b < P.B && active) {
+      int a = a0;
+      for (int i = 0; i <= k; ++i) {
+        const int gx = i < k ? P.draft_tokens[d0 + i] : -1;
+        w.rowlist[a++] = make_int4(t0 + i, b, gx, (i << 2) | mode_t);
+      }
+      if (mode_d != kSkip)
+        for (int i = 0; i < k; ++i)
+          w.rowlist[a++] =
+              make_int4((int)P.Rt + d0 + i, b, P.draft_tokens[d0 + i], (i << 2) | mode_d);
+    }
+    if (b < P.B && (code || mode_d == kSkip)) {
+      // Rows the streaming pass will not visit still get a defined record.
+      for (int i = 0; i < k; ++i) {
+        RowStat& st = w.stats[P.Rt + d0 + i];
+        st.s = 0.0;
+        st.pg = __longlong_as_double(0x7ff8000000000000LL);
+        st.m = 0.0f;
+        st.arg = -1;
+        st.kept = 0;
+        st.mode = kSkip;
+      }
+    }
+  }
+  if (threadIdx.x == 0) w.hdr->n_active = carry_a;
+}
+
+}  // namespace
+
+cudaError_t launch_setup(const Problem& P, cudaStream_t s) {
+  setup_kernel<<<1, kSetupThreads, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace sv
