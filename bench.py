@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--config", default="c4")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (small cases for profiling; not a bench line)")
     return ap.parse_args()
 
 
@@ -218,6 +221,51 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def measure_e2e(args, batch, v, acc, tok, stream, dev, pg):
+    """Same metric through the public API from pinned host buffers: every step
+    copies the step's inputs host->device and reads the results back."""
+    import torch
+    ws = pg.get_world_size() if pg else 1
+    B, Rt = batch.batch, batch.target_rows
+    host = {k: getattr(batch, k).to("cpu").pin_memory() for k in
+            ("target", "draft", "draft_tokens", "k_per_req", "temperature", "top_k", "top_p",
+             "uniforms")}
+    dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    tok_h = torch.empty(Rt, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
+
+    def e2e_step():
+        for k_, t in host.items():
+            dbuf[k_].copy_(t, non_blocking=True)
+        a, o = v(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["k_per_req"],
+                 dbuf["temperature"], dbuf["uniforms"], dbuf["top_k"], dbuf["top_p"],
+                 out_accept_len=acc, out_tokens=tok)
+        acc_h.copy_(a, non_blocking=True)
+        tok_h.copy_(o, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    del dbuf, host
+    return {"value": ws * Rt / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms}
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
@@ -242,7 +290,7 @@ def main():
         pg.barrier()
     sv.load_library()
 
-    batch = workloads.make_batch(args.config, device=dev, seed_offset=rank)
+    batch = workloads.make_batch(args.config, device=dev, seed_offset=rank, batch=args.batch)
     B, Rt, Rd, V = batch.batch, batch.target_rows, batch.draft_rows, batch.vocab
     bytes_per_step = batch.logit_bytes()
     v = sv.Verifier(dev)
@@ -284,43 +332,7 @@ def main():
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         step_ms = float(t.item())
 
-    # end to end through the public API from pinned host buffers
-    host = {k: getattr(batch, k).to("cpu").pin_memory() for k in
-            ("target", "draft", "draft_tokens", "k_per_req", "temperature", "top_k", "top_p",
-             "uniforms")}
-    dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
-    acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
-    tok_h = torch.empty(Rt, dtype=torch.int32).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = acc_h.numel() * 4 + tok_h.numel() * 4
-
-    def e2e_step():
-        for k_, t in host.items():
-            dbuf[k_].copy_(t, non_blocking=True)
-        a, o = v(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["k_per_req"],
-                 dbuf["temperature"], dbuf["uniforms"], dbuf["top_k"], dbuf["top_p"],
-                 out_accept_len=acc, out_tokens=tok)
-        acc_h.copy_(a, non_blocking=True)
-        tok_h.copy_(o, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    del dbuf, host
-
+    e2e = None if args.no_e2e else measure_e2e(args, batch, v, acc, tok, stream, dev, pg)
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -354,8 +366,7 @@ def main():
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": peak_src,
                      "bytes_per_launch": bytes_per_step, "launch_ms": rowpass_ms},
-        "e2e": {"value": ws * Rt / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms},
+        "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

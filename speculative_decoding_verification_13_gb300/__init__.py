@@ -121,6 +121,16 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _event_handle(ev, stream):
+    """cudaEvent_t of a torch.cuda.Event (torch creates the event lazily on its
+    first record; the library re-records it where the row pass starts / ends)."""
+    if ev is None:
+        return None
+    if ev.cuda_event == 0:
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+    return ctypes.c_void_p(ev.cuda_event)
+
+
 def _check(t, name, dtype, ndim=1):
     if t is None:
         return
@@ -196,9 +206,7 @@ class Verifier:
         opts = None
         if out_pq is not None or rowpass_events is not None:
             ev0, ev1 = rowpass_events if rowpass_events is not None else (None, None)
-            opts = _Options(_ptr(out_pq),
-                            ctypes.c_void_p(ev0.cuda_event) if ev0 is not None else None,
-                            ctypes.c_void_p(ev1.cuda_event) if ev1 is not None else None)
+            opts = _Options(_ptr(out_pq), _event_handle(ev0, stream), _event_handle(ev1, stream))
         rc = lib.spec_verify(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
                              _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
                              _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),

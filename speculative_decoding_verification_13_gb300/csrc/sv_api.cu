@@ -116,7 +116,8 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_setup(P, s) != cudaSuccess) return SV_ERR_CUDA;
   const int64_t rows = t.rows + d.rows;
-  const int grid = int(rows < sms ? rows : sms);
+  const int64_t ctas = int64_t(sms) * kRowpassCtasPerSm;
+  const int grid = int(rows < ctas ? rows : ctas);
   if (options && options->event_rowpass_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
     return SV_ERR_CUDA;

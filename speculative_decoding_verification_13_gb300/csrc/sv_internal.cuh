@@ -11,12 +11,14 @@
 namespace sv {
 
 // ---------------------------------------------------------------- constants
-constexpr int kConsumerWarps = 16;                       // warps that read tiles
-constexpr int kConsumers = kConsumerWarps * 32;          // 512 threads
+constexpr int kConsumerWarps = 8;                        // warps that read tiles
+constexpr int kConsumers = kConsumerWarps * 32;          // 256 threads
 constexpr int kRowpassThreads = kConsumers + 32;         // + one producer warp
+constexpr int kRowpassCtasPerSm = 2;                     // one CTA's epilogue overlaps
+                                                         // the other's streaming
 constexpr int kTileBytes = 16384;                        // one bulk copy
-constexpr int kStages = 8;                               // smem ring depth
-constexpr int kBufCap = 4096;                            // top-k candidate buffer
+constexpr int kStages = 4;                               // smem ring depth per CTA
+constexpr int kBufCap = 2560;                            // top-k candidate buffer
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr int kFinalThreads = 256;

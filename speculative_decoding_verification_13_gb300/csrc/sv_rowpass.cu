@@ -36,13 +36,15 @@ constexpr size_t kOffScratch = kOffBuf + size_t(kBufCap) * 8;
 constexpr size_t kOffXchg = kOffScratch + size_t(kScratch) * 8;
 constexpr size_t kOffBars = kOffXchg + size_t(2 * kConsumers) * 8;
 constexpr size_t kSmemBytes = kOffBars + size_t(2 * kStages) * 8;
-static_assert(kSmemBytes + 8192 <= 227 * 1024, "shared memory budget");
+static_assert(kRowpassCtasPerSm * (kSmemBytes + 4096 + 1024) <= 228 * 1024,
+              "shared memory budget for the resident CTAs of one SM");
 
 struct RowShared {
   int hist[256];
   SelShared sel;
   unsigned long long theta;
-  unsigned int pend[2];
+  unsigned int bnd[2];
+  unsigned int ins[2];
   int count;
   int tmpcount;
   int cabort;
@@ -119,7 +121,7 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kRowpassThreads, 1) rowpass_kernel(const Problem P) {
+__global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_kernel(const Problem P) {
   using E = Elt<BF16>;
   constexpr int EPV = E::kPerVec;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -142,7 +144,8 @@ __global__ void __launch_bounds__(kRowpassThreads, 1) rowpass_kernel(const Probl
     S.cabort = 0;
     S.pabort = 0;
     S.count = 0;
-    S.pend[0] = S.pend[1] = 0u;
+    S.bnd[0] = S.bnd[1] = 0u;
+    S.ins[0] = S.ins[1] = 0u;
     S.bad = 0;
     S.theta = 0ull;
   }
@@ -203,8 +206,9 @@ __global__ void __launch_bounds__(kRowpassThreads, 1) rowpass_kernel(const Probl
   // ------------------------------------------------------------- consumers
   const int ctid = tid - 32, cwarp = warp - 1;
   uint32_t stage = 0, phase = 0;
-  unsigned int pend_seen[2] = {0u, 0u};
-  int pend_sel = 0;
+  unsigned bnd_seen[2] = {0u, 0u};
+  unsigned ins_seen[2] = {0u, 0u};
+  unsigned gtile = 0;  // tiles consumed by this CTA (parity of the tally counters)
 
   auto acquire = [&]() -> const uint4* {
     if (!wait_or_abort(full0 + 8u * stage, phase, &S.cabort, &S.pabort)) {
@@ -387,73 +391,116 @@ __global__ void __launch_bounds__(kRowpassThreads, 1) rowpass_kernel(const Probl
       }
     } else {
       // ---------------------------------------------- top-k / top-p
+      // Per tile: phase A flags the vectors whose maximum reaches the
+      // threshold (packed max, no decoding) and tallies an upper bound of the
+      // candidates; one barrier; phase B reads the flagged vectors back from
+      // shared memory GROUP at a time (EPV lanes per vector, so a warp never
+      // runs a per-lane slow path) and appends the elements that beat the
+      // threshold.  Exact fill counts travel through monotone counters that
+      // alternate with the tile parity, so no second barrier is needed.
       const int K = P.top_k[b];
       const float tp = P.top_p ? P.top_p[b] : 1.0f;
-      int count = 0;  // buffer fill, identical in every consumer thread
+      constexpr uint32_t kSkip = BF16 ? kSkipBf16 : kSkipF32;
+      constexpr int VPT = (kTileBytes / 16 + kConsumers - 1) / kConsumers;
+      constexpr int GROUP = 32 / EPV;
+      int count = 0;  // exact buffer fill at the last tile boundary (uniform)
       bool bad = false;
-      int cnt = 0;    // this thread's candidates in the current tile
 
-      // Candidates of this thread's vectors at threshold th (composite order).
-      auto count_pass = [&](const uint4* tile, int nvec, int t, uint64_t th) {
-        const float thv = composite_value(th);
-        int c = 0;
-        for (int v = ctid; v < nvec; v += kConsumers) {
-          const uint4 q = tile[v];
-          if (!(E::vmax(q) < thv)) {
-            float x[EPV];
-            E::decode(q, x);
-            const uint32_t i0 = uint32_t(t * kTileElems + v * EPV);
-            for (int e = 0; e < EPV; ++e) {
-              if (x[e] != x[e] || x[e] == INFINITY) bad = true;
-              else if (composite_key(x[e], i0 + e) >= th) ++c;
-            }
-          }
-        }
-        return c;
-      };
-      // Adds this tile's count to the shared pending counter; returns the
-      // CTA total (identical in all threads).
-      auto tally = [&](int c) -> int {
-        int ws = c;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-        if (lane == 0 && ws) atomicAdd(&S.pend[pend_sel], unsigned(ws));
+      auto tally = [&](unsigned* ctr, unsigned& seen, unsigned wv) -> int {
+        if (lane == 0 && wv) atomicAdd(ctr, wv);
         consumer_sync();
-        const unsigned now = *reinterpret_cast<volatile unsigned*>(&S.pend[pend_sel]);
-        const int tot = int(now - pend_seen[pend_sel]);
-        pend_seen[pend_sel] = now;
+        const unsigned now = *reinterpret_cast<volatile unsigned*>(ctr);
+        const int tot = int(now - seen);
+        seen = now;
         return tot;
       };
-      // k-th largest per-vector maximum of this tile: a threshold at or below
-      // the k-th largest element of the row.
+      auto phase_a = [&](const uint4* tile, int nvec, float thv, uint32_t& cbits) -> unsigned {
+        cbits = 0u;
+        unsigned nb = 0;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = ctid + i * kConsumers;
+          const bool c = v < nvec && !(E::vmax(tile[v]) < thv);
+          nb += __popc(__ballot_sync(0xffffffffu, c));
+          if (c) cbits |= 1u << i;
+        }
+        return nb * EPV;
+      };
+      auto phase_b = [&](const uint4* tile, int t, uint32_t cbits, uint64_t th) -> unsigned {
+        unsigned ins = 0;
+        const int g = lane / EPV, e = lane % EPV;
+        const char* tb = reinterpret_cast<const char*>(tile);
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          uint32_t m = __ballot_sync(0xffffffffu, (cbits >> i) & 1u);
+          while (m) {
+            uint32_t mg = m;
+            for (int j = 0; j < g; ++j) mg &= mg - 1u;  // drop g lowest set bits
+            const bool has = mg != 0u;
+            uint64_t key = 0ull;
+            bool pass = false;
+            if (has) {
+              const int v = cwarp * 32 + (__ffs(mg) - 1) + i * kConsumers;
+              float x;
+              if (BF16)
+                x = __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(
+                                        tb + size_t(v) * 16 + e * 2)) << 16);
+              else
+                x = *reinterpret_cast<const float*>(tb + size_t(v) * 16 + e * 4);
+              if (x != x || x == INFINITY) {
+                bad = true;
+              } else {
+                key = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
+                pass = key >= th;
+              }
+            }
+            const uint32_t pm = __ballot_sync(0xffffffffu, pass);
+            const int np = __popc(pm);
+            int base = 0;
+            if (lane == 0 && np) base = atomicAdd(&S.count, np);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (pass) {
+              const int slot = base + __popc(pm & ((1u << lane) - 1u));
+              if (slot < kBufCap) buf[slot] = key;
+            }
+            ins += unsigned(np);
+#pragma unroll
+            for (int j = 0; j < GROUP; ++j) m &= m - 1u;
+          }
+        }
+        return ins;
+      };
+      // Threshold from this tile: the K-th largest per-vector maximum (the
+      // maximum taken in the same composite order), a lower bound of the
+      // row's K-th largest element.
       auto bootstrap = [&](const uint4* tile, int nvec, int t) {
         for (int v = ctid; v < nvec; v += kConsumers) {
+          const uint4 q = tile[v];
+          const float vm = E::vmax(q);
           float x[EPV];
-          E::decode(tile[v], x);
-          const uint32_t i0 = uint32_t(t * kTileElems + v * EPV);
-          uint64_t mx = 0ull;
-          for (int e = 0; e < EPV; ++e) {
-            const uint64_t c = composite_key(x[e], i0 + e);
-            mx = c > mx ? c : mx;
-          }
-          scratch[v] = mx;
+          E::decode(q, x);
+          int first = 0;
+          for (int e = EPV - 1; e >= 0; --e)
+            if (x[e] == vm) first = e;
+          scratch[v] = composite_key(vm, uint32_t(t * kTileElems + v * EPV + first));
         }
         consumer_sync();
-        const uint64_t tb =
-            block_select_kth<kConsumers>(scratch, nvec, K, ctid, S.hist, &S.sel, ConsumerSync());
+        const uint64_t tb = block_select_kth<kConsumers>(scratch, nvec, K, ctid, S.hist, &S.sel,
+                                                         ConsumerSync(), kSkip);
         if (ctid == 0 && tb > S.theta) S.theta = tb;
         consumer_sync();
       };
-      // Keep exactly the K largest buffer entries; the K-th becomes the threshold.
-      auto compact = [&]() {
-        const uint64_t th =
-            block_select_kth<kConsumers>(buf, count, K, ctid, S.hist, &S.sel, ConsumerSync());
+      // Keep exactly the K largest of the n buffered candidates; the K-th
+      // becomes the threshold.
+      auto compact = [&](int n) {
+        const uint64_t th = block_select_kth<kConsumers>(buf, n, K, ctid, S.hist, &S.sel,
+                                                         ConsumerSync(), kSkip);
         if (ctid == 0) S.tmpcount = 0;
         consumer_sync();
-        for (int base = cwarp * 32; base < count; base += kConsumers) {
+        for (int base = cwarp * 32; base < n; base += kConsumers) {
           const int e = base + lane;
-          const uint64_t key = e < count ? buf[e] : 0ull;
-          const bool keep = e < count && key >= th;
+          const uint64_t key = e < n ? buf[e] : 0ull;
+          const bool keep = e < n && key >= th;
           const uint32_t bal = __ballot_sync(0xffffffffu, keep);
           int slot0 = 0;
           if (lane == 0 && bal) slot0 = atomicAdd(&S.tmpcount, __popc(bal));
@@ -469,106 +516,72 @@ __global__ void __launch_bounds__(kRowpassThreads, 1) rowpass_kernel(const Probl
           S.count = K;
           if (th > S.theta) S.theta = th;
         }
-        count = K;
         consumer_sync();
-      };
-      // Writes this thread's candidates at threshold th into the buffer.
-      auto insert = [&](const uint4* tile, int nvec, int t, uint64_t th, int c) {
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-        int base = 0;
-        if (lane == 31 && wtot) base = atomicAdd(&S.count, wtot);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        int slot = base + incl - c;
-        if (c == 0) return;
-        const float thv = composite_value(th);
-        for (int v = ctid; v < nvec; v += kConsumers) {
-          const uint4 q = tile[v];
-          if (!(E::vmax(q) < thv)) {
-            float x[EPV];
-            E::decode(q, x);
-            const uint32_t i0 = uint32_t(t * kTileElems + v * EPV);
-            for (int e = 0; e < EPV; ++e) {
-              if (x[e] != x[e] || x[e] == INFINITY) continue;
-              const uint64_t key = composite_key(x[e], i0 + e);
-              if (key >= th) {
-                if (slot < kBufCap) buf[slot] = key;
-                ++slot;
-              }
-            }
-          }
-        }
       };
 
       for (int t = 0; t < ntiles; ++t) {
         const uint4* tile = acquire();
         const int nvec = tile_vectors(t);
+        const int par = int(gtile & 1u);
+        const int prev = par ^ 1;
         if (t == 0 && nvec >= K) bootstrap(tile, nvec, t);
         uint64_t th = S.theta;
-        cnt = count_pass(tile, nvec, t, th);
-        int pend = tally(cnt);
-        if (count + pend > kBufCap - 8) {
+        uint32_t cbits;
+        unsigned wb = phase_a(tile, nvec, composite_value(th), cbits);
+        int bound = tally(&S.bnd[par], bnd_seen[par], wb);
+        if (t > 0) {
+          // insertions of the previous tile are complete once every warp passed the barrier
+          const unsigned now = *reinterpret_cast<volatile unsigned*>(&S.ins[prev]);
+          count += int(now - ins_seen[prev]);
+          ins_seen[prev] = now;
+        }
+        if (count + bound > kBufCap - 8) {  // rare: make room first
           consumer_sync();
-          if (count > K) compact();
+          if (count > K) {
+            compact(count);
+            count = K;
+          }
           th = S.theta;
-          cnt = count_pass(tile, nvec, t, th);
-          pend = tally(cnt);
-          if (count + pend > kBufCap - 8 && nvec >= K) {
-            consumer_sync();
+          wb = phase_a(tile, nvec, composite_value(th), cbits);
+          bound = tally(&S.bnd[par], bnd_seen[par], wb);
+          if (count + bound > kBufCap - 8 && nvec >= K) {
             bootstrap(tile, nvec, t);
             th = S.theta;
-            cnt = count_pass(tile, nvec, t, th);
-            pend = tally(cnt);
+            wb = phase_a(tile, nvec, composite_value(th), cbits);
+            bound = tally(&S.bnd[par], bnd_seen[par], wb);
           }
         }
-        if (pend > 0) insert(tile, nvec, t, th, cnt);
-        count += pend;
-        if (count > kBufCap) {  // cannot happen (capacity bound); never read past the buffer
-          if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
-          count = kBufCap;
-        }
-        pend_sel ^= 1;
+        const unsigned ins = phase_b(tile, t, cbits, th);
+        if (lane == 0 && ins) atomicAdd(&S.ins[par], ins);
         release();
+        ++gtile;
       }
       // ragged tail (fewer than 16 bytes), read directly from global memory
-      if (n_tail > 0) {
-        const uint64_t th = S.theta;
-        bool pass = false;
-        uint64_t key = 0ull;
-        if (ctid < n_tail) {
-          const float x = E::scalar(rowp, tail_start + ctid);
-          if (x != x || x == INFINITY) bad = true;
-          else {
-            key = composite_key(x, uint32_t(tail_start + ctid));
-            pass = key >= th;
+      if (ctid < n_tail) {
+        const float x = E::scalar(rowp, tail_start + ctid);
+        if (x != x || x == INFINITY) {
+          bad = true;
+        } else {
+          const uint64_t key = composite_key(x, uint32_t(tail_start + ctid));
+          if (key >= S.theta) {
+            const int slot = atomicAdd(&S.count, 1);
+            if (slot < kBufCap) buf[slot] = key;
           }
         }
-        const int pend = tally(pass ? 1 : 0);
-        const uint32_t bal = __ballot_sync(0xffffffffu, pass);
-        if (cwarp == 0 && pass) {
-          const int slot = count + __popc(bal & ((1u << lane) - 1u));
-          if (slot < kBufCap) buf[slot] = key;
-        }
-        count += pend;
-        if (count > kBufCap) {
-          if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
-          count = kBufCap;
-        }
-        pend_sel ^= 1;
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad, 1);
       consumer_sync();
+      count = *reinterpret_cast<volatile int*>(&S.count);
+      ins_seen[0] = *reinterpret_cast<volatile unsigned*>(&S.ins[0]);
+      ins_seen[1] = *reinterpret_cast<volatile unsigned*>(&S.ins[1]);
+      if (count > kBufCap) {  // cannot happen (capacity bound); never read past the buffer
+        if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
+        count = kBufCap;
+      }
 
       // final selection: exactly min(count, K) survivors, sorted descending
       const int nsel = count < K ? count : K;
-      if (count > K) {
-        compact();  // leaves the K largest in buf[0..K)
-      }
+      if (count > K) compact(count);  // leaves the K largest in buf[0..K)
       const int Psz = next_pow2(nsel > 0 ? nsel : 1);
       uint64_t v = (ctid < nsel) ? buf[ctid] : 0ull;
       v = block_sort_desc<kConsumers>(v, ctid, Psz, xchg, ConsumerSync());

@@ -22,13 +22,21 @@ struct SelShared {
   unsigned long long minv;
 };
 
+// Digit positions (shift / 8) that hold the same byte in every key can be
+// skipped: bit s of `skip` skips the digit at shift 8 * s.  For keys built
+// from bfloat16 values the low 16 bits of the value word are constant, and for
+// indices below 2^24 the top byte of ~index is constant.
+constexpr uint32_t kSkipBf16 = (1u << 5) | (1u << 4) | (1u << 3);
+constexpr uint32_t kSkipF32 = (1u << 3);
+
 template <int NT, class Sync>
 __device__ uint64_t block_select_kth(const uint64_t* keys, int n, int k, int tid, int* hist,
-                                     SelShared* sh, Sync sync) {
+                                     SelShared* sh, Sync sync, uint32_t skip = 0) {
   const int lane = tid & 31, warp = tid >> 5;
   uint64_t prefix = 0, mask = 0;
   int need = k;
   for (int shift = 56; shift >= 0; shift -= 8) {
+    if ((skip >> (shift / 8)) & 1u) continue;
     for (int i = tid; i < 256; i += NT) hist[i] = 0;
     if (tid == 0) sh->minv = ~0ull;
     sync();

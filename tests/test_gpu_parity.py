@@ -118,10 +118,24 @@ def test_filtered_kept_sets_match_oracle():
 
 # ---------------------------------------------------------------- edge cases
 
+def padded(x):
+    """Same values in a [rows, V] view whose row stride is a multiple of 16
+    bytes (the library's alignment contract for TMA row copies)."""
+    per = 16 // x.element_size()
+    Vp = (x.shape[1] + per - 1) // per * per
+    if Vp == x.shape[1]:
+        return x
+    y = torch.full((x.shape[0], Vp), float("nan"), dtype=x.dtype, device=x.device)
+    y[:, :x.shape[1]] = x
+    return y[:, :x.shape[1]]
+
+
 def custom(k, T, V, dtype=torch.bfloat16, top_k=None, top_p=None, sig=1.0, seed=5):
     B = len(k)
-    return W.make_batch_from_params("edge", k, T, [sig] * B, V, dtype, seed, device=DEV,
-                                    top_k=top_k, top_p=top_p)
+    b = W.make_batch_from_params("edge", k, T, [sig] * B, V, dtype, seed, device=DEV,
+                                 top_k=top_k, top_p=top_p)
+    b.target, b.draft = padded(b.target), padded(b.draft)
+    return b
 
 
 @pytest.mark.parametrize("V", [1, 3, 7, 8, 9, 1000, 4097, 8193, 40000])
@@ -134,6 +148,12 @@ def test_vocab_sizes_and_ragged_tails(V, dtype):
         tk = [min(5, V - 1)] * 5
         check(custom(k, [1.0, 0.7, 1.0, 2.0, 0.0], V, dtype, top_k=tk, top_p=[0.9] * 5),
               f"V={V} filtered")
+
+
+def test_unaligned_row_stride_is_rejected_on_the_host():
+    b = W.make_batch_from_params("edge", [1], [1.0], [1.0], 3, torch.float32, 5, device=DEV)
+    with pytest.raises(sv.SpecVerifyError, match="UNSUPPORTED"):
+        run_gpu(b)
 
 
 def test_k_extremes_and_ragged_mix():
@@ -152,6 +172,8 @@ def test_identical_target_and_draft_accepts_everything():
     for r in range(3):
         for i in range(7):
             b.draft[t_off[r] - r + i] = b.target[t_off[r] + i]
+            # the argmax survives every filter, so p(x) = q(x) > 0
+            b.draft_tokens[t_off[r] - r + i] = torch.argmax(b.target[t_off[r] + i])
     g, o, _ = check(b, "p == q")
     assert (g["acc"] == 7).all()
 
