@@ -19,6 +19,7 @@ constexpr int kRowpassCtasPerSm = 2;                     // one CTA's epilogue o
 constexpr int kTileBytes = 16384;                        // one bulk copy
 constexpr int kStages = 4;                               // smem ring depth per CTA
 constexpr int kBufCap = 2560;                            // top-k candidate buffer
+constexpr int kRegion = kBufCap / kConsumerWarps;        // per-warp region (fast path)
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr int kFinalThreads = 256;

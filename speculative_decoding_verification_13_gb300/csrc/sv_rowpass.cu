@@ -42,15 +42,17 @@ static_assert(kRowpassCtasPerSm * (kSmemBytes + 4096 + 1024) <= 228 * 1024,
 struct RowShared {
   int hist[256];
   SelShared sel;
-  unsigned long long theta;
+  unsigned long long thmin[3];
   unsigned int bnd[2];
   unsigned int ins[2];
   int count;
   int tmpcount;
+  int ovf;
   int cabort;
   int pabort;
   int bad;
   int kp;
+  int wcnt[kConsumerWarps];
   float v0;
   double wp;
   double pg;
@@ -103,15 +105,33 @@ struct Elt<false> {
   }
 };
 
+// Bounded wait with back-off: a waiting warp sleeps between polls so that it
+// does not take issue slots from the warps that do the work.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const int* f1,
-                                              const int* f2) {
+                                              const int* f2, uint32_t sleep_ns) {
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 255u &&
         (*reinterpret_cast<const volatile int*>(f1) || *reinterpret_cast<const volatile int*>(f2)))
       return false;
+    __nanosleep(sleep_ns);
   }
   return false;
+}
+
+// Position of the n-th (0-based) set bit of x; x must hold more than n set bits.
+__device__ __forceinline__ int nth_set_bit(uint32_t x, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) {
+    const int c = __popc(x & ((1u << w) - 1u));
+    if (n >= c) {
+      n -= c;
+      x >>= w;
+      pos += w;
+    }
+  }
+  return pos;
 }
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -144,10 +164,12 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     S.cabort = 0;
     S.pabort = 0;
     S.count = 0;
+    S.ovf = 0;
     S.bnd[0] = S.bnd[1] = 0u;
     S.ins[0] = S.ins[1] = 0u;
     S.bad = 0;
-    S.theta = 0ull;
+    S.thmin[0] = S.thmin[1] = ~0ull;
+    S.tmpcount = 0;
   }
   __syncthreads();
 
@@ -175,7 +197,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       for (int t = 0; t < ntiles; ++t) {
         const int64_t rem = bulk - int64_t(t) * kTileBytes;
         const uint32_t bytes = uint32_t(rem < kTileBytes ? rem : kTileBytes);
-        if (!wait_or_abort(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort)) {
+        if (!wait_or_abort(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
           *reinterpret_cast<volatile int*>(&S.pabort) = 1;
           record_error(w.hdr, SV_ERR_TIMEOUT, -1, row);
           stop = true;
@@ -209,9 +231,10 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
   unsigned bnd_seen[2] = {0u, 0u};
   unsigned ins_seen[2] = {0u, 0u};
   unsigned gtile = 0;  // tiles consumed by this CTA (parity of the tally counters)
+  int tsel = 0;        // which of the two CTA-minimum slots is live
 
   auto acquire = [&]() -> const uint4* {
-    if (!wait_or_abort(full0 + 8u * stage, phase, &S.cabort, &S.pabort)) {
+    if (!wait_or_abort(full0 + 8u * stage, phase, &S.cabort, &S.pabort, 16)) {
       *reinterpret_cast<volatile int*>(&S.cabort) = 1;
       record_error(w.hdr, SV_ERR_TIMEOUT, -1, -1);
     }
@@ -391,20 +414,32 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       }
     } else {
       // ---------------------------------------------- top-k / top-p
-      // Per tile: phase A flags the vectors whose maximum reaches the
-      // threshold (packed max, no decoding) and tallies an upper bound of the
-      // candidates; one barrier; phase B reads the flagged vectors back from
-      // shared memory GROUP at a time (EPV lanes per vector, so a warp never
-      // runs a per-lane slow path) and appends the elements that beat the
-      // threshold.  Exact fill counts travel through monotone counters that
-      // alternate with the tile parity, so no second barrier is needed.
+      // Fast path (one pass, no per-tile barrier): a speculative threshold is
+      // taken from tile 0 -- a rank there that the row's top K exceed only
+      // with negligible probability (tile 0 holds about lambda = K * |tile| / V
+      // of them; rank lambda + 4 sqrt(lambda) + 4) -- and every element at or
+      // above it is appended to a shared buffer.  At the end of the row the
+      // speculation is verified: if nothing overflowed and at least K
+      // elements passed, the row's top K are all in the buffer.  Otherwise
+      // the row is streamed again from global memory by the certified path:
+      // per tile, phase A flags the vectors whose maximum reaches the
+      // threshold and tallies an upper bound of the candidates, one barrier
+      // checks the buffer capacity (compacting to the exact K largest when
+      // needed), and phase B inserts.
+      //
+      // Thresholds: each warp takes the m-th largest of the keys it holds and
+      // the CTA takes the minimum, so at least 8m keys reach it.
       const int K = P.top_k[b];
       const float tp = P.top_p ? P.top_p[b] : 1.0f;
       constexpr uint32_t kSkip = BF16 ? kSkipBf16 : kSkipF32;
       constexpr int VPT = (kTileBytes / 16 + kConsumers - 1) / kConsumers;
       constexpr int GROUP = 32 / EPV;
-      int count = 0;  // exact buffer fill at the last tile boundary (uniform)
+      constexpr int UNR = 2;
+      const int m = (K + kConsumerWarps - 1) / kConsumerWarps;
+      uint64_t theta = 0ull;  // uniform
+      int count = 0;          // exact buffer fill at the last tile boundary (uniform)
       bool bad = false;
+      bool redo = false;      // the speculative pass must be redone by the certified path
 
       auto tally = [&](unsigned* ctr, unsigned& seen, unsigned wv) -> int {
         if (lane == 0 && wv) atomicAdd(ctr, wv);
@@ -413,6 +448,15 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         const int tot = int(now - seen);
         seen = now;
         return tot;
+      };
+      // CTA minimum of the per-warp values (one barrier).
+      auto cta_min = [&](uint64_t wv) -> uint64_t {
+        if (lane == 0) atomicMin(&S.thmin[tsel], static_cast<unsigned long long>(wv));
+        consumer_sync();
+        const uint64_t r = *reinterpret_cast<volatile unsigned long long*>(&S.thmin[tsel]);
+        if (ctid == 0) S.thmin[tsel ^ 1] = ~0ull;
+        tsel ^= 1;
+        return r;
       };
       auto phase_a = [&](const uint4* tile, int nvec, float thv, uint32_t& cbits) -> unsigned {
         cbits = 0u;
@@ -426,72 +470,233 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         }
         return nb * EPV;
       };
+      auto element = [&](const char* tb, int v, int e) -> float {
+        if (BF16)
+          return __uint_as_float(
+              uint32_t(*reinterpret_cast<const uint16_t*>(tb + size_t(v) * 16 + e * 2)) << 16);
+        return *reinterpret_cast<const float*>(tb + size_t(v) * 16 + e * 4);
+      };
       auto phase_b = [&](const uint4* tile, int t, uint32_t cbits, uint64_t th) -> unsigned {
-        unsigned ins = 0;
         const int g = lane / EPV, e = lane % EPV;
         const char* tb = reinterpret_cast<const char*>(tile);
+        uint64_t key[VPT][UNR];
+        uint32_t pm[VPT][UNR];
+        uint32_t rest[VPT];
+        int tot = 0;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-          uint32_t m = __ballot_sync(0xffffffffu, (cbits >> i) & 1u);
-          while (m) {
-            uint32_t mg = m;
-            for (int j = 0; j < g; ++j) mg &= mg - 1u;  // drop g lowest set bits
-            const bool has = mg != 0u;
-            uint64_t key = 0ull;
+          uint32_t mm = __ballot_sync(0xffffffffu, (cbits >> i) & 1u);
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            key[i][u] = 0ull;
+            pm[i][u] = 0u;
+            if (mm) {
+              uint32_t mg = mm;
+              for (int j = 0; j < g; ++j) mg &= mg - 1u;  // the g-th flagged vector
+              bool pass = false;
+              if (mg) {
+                const int v = cwarp * 32 + (__ffs(mg) - 1) + i * kConsumers;
+                const float x = element(tb, v, e);
+                if (x != x || x == INFINITY) {
+                  bad = true;
+                } else {
+                  key[i][u] = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
+                  pass = key[i][u] >= th;
+                }
+              }
+              pm[i][u] = __ballot_sync(0xffffffffu, pass);
+              tot += __popc(pm[i][u]);
+#pragma unroll
+              for (int j = 0; j < GROUP; ++j) mm &= mm - 1u;
+            }
+          }
+          rest[i] = mm;
+        }
+        int base = 0;
+        if (lane == 0 && tot) base = atomicAdd(&S.count, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+#pragma unroll
+          for (int u = 0; u < UNR; ++u) {
+            if ((pm[i][u] >> lane) & 1u) {
+              const int slot = base + __popc(pm[i][u] & lt);
+              if (slot < kBufCap) buf[slot] = key[i][u];
+            }
+            base += __popc(pm[i][u]);
+          }
+        unsigned ins = unsigned(tot);
+        // rare: a vector slot with more than UNR groups of flagged vectors
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          uint32_t mm = rest[i];
+          while (mm) {
+            uint32_t mg = mm;
+            for (int j = 0; j < g; ++j) mg &= mg - 1u;
+            uint64_t k1 = 0ull;
             bool pass = false;
-            if (has) {
+            if (mg) {
               const int v = cwarp * 32 + (__ffs(mg) - 1) + i * kConsumers;
-              float x;
-              if (BF16)
-                x = __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(
-                                        tb + size_t(v) * 16 + e * 2)) << 16);
-              else
-                x = *reinterpret_cast<const float*>(tb + size_t(v) * 16 + e * 4);
+              const float x = element(tb, v, e);
               if (x != x || x == INFINITY) {
                 bad = true;
               } else {
-                key = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
-                pass = key >= th;
+                k1 = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
+                pass = k1 >= th;
               }
             }
-            const uint32_t pm = __ballot_sync(0xffffffffu, pass);
-            const int np = __popc(pm);
-            int base = 0;
-            if (lane == 0 && np) base = atomicAdd(&S.count, np);
-            base = __shfl_sync(0xffffffffu, base, 0);
+            const uint32_t pb = __ballot_sync(0xffffffffu, pass);
+            const int np = __popc(pb);
+            int b1 = 0;
+            if (lane == 0 && np) b1 = atomicAdd(&S.count, np);
+            b1 = __shfl_sync(0xffffffffu, b1, 0);
             if (pass) {
-              const int slot = base + __popc(pm & ((1u << lane) - 1u));
-              if (slot < kBufCap) buf[slot] = key;
+              const int slot = b1 + __popc(pb & lt);
+              if (slot < kBufCap) buf[slot] = k1;
             }
             ins += unsigned(np);
 #pragma unroll
-            for (int j = 0; j < GROUP; ++j) m &= m - 1u;
+            for (int j = 0; j < GROUP; ++j) mm &= mm - 1u;
           }
         }
         return ins;
       };
-      // Threshold from this tile: the K-th largest per-vector maximum (the
-      // maximum taken in the same composite order), a lower bound of the
-      // row's K-th largest element.
-      auto bootstrap = [&](const uint4* tile, int nvec, int t) {
-        for (int v = ctid; v < nvec; v += kConsumers) {
-          const uint4 q = tile[v];
-          const float vm = E::vmax(q);
-          float x[EPV];
-          E::decode(q, x);
-          int first = 0;
-          for (int e = EPV - 1; e >= 0; --e)
-            if (x[e] == vm) first = e;
-          scratch[v] = composite_key(vm, uint32_t(t * kTileElems + v * EPV + first));
+      // Fast path: flag the tile's vectors with a packed max, then decode the
+      // flagged ones GROUP at a time (EPV lanes per vector) and append the
+      // passing elements to this warp's own buffer region.  No atomics and no
+      // barrier; a region overflow marks the row for the certified redo.
+      uint64_t* region = buf + cwarp * kRegion;
+      int wcnt = 0;  // fill of this warp's region (warp-uniform)
+      auto fused_pass = [&](const uint4* tile, int nvec, int t, uint64_t th) {
+        const float thv = composite_value(th);
+        uint32_t mk[VPT];
+        int total = 0;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v0 = ctid + i * kConsumers;
+          const bool c = v0 < nvec && !(E::vmax(tile[v0]) < thv);
+          mk[i] = __ballot_sync(0xffffffffu, c);
+          total += __popc(mk[i]);
         }
+        if (total == 0) return;
+        const int g = lane / EPV, e = lane % EPV;
+        const char* tb = reinterpret_cast<const char*>(tile);
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int b0 = 0; b0 < total; b0 += GROUP) {
+          int n = b0 + g;
+          uint64_t key = 0ull;
+          bool pass = false;
+          if (n < total) {
+            int slot = 0;
+            uint32_t bits = mk[0];
+            bool found = false;
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+              const int c = __popc(mk[i]);
+              if (!found) {
+                if (n < c) {
+                  found = true;
+                  slot = i;
+                  bits = mk[i];
+                } else {
+                  n -= c;
+                }
+              }
+            }
+            const int v = cwarp * 32 + nth_set_bit(bits, n) + slot * kConsumers;
+            const float x = element(tb, v, e);
+            if (x != x || x == INFINITY) {
+              bad = true;
+            } else {
+              key = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
+              pass = key >= th;
+            }
+          }
+          const uint32_t pm = __ballot_sync(0xffffffffu, pass);
+          if (pass) {
+            const int sidx = wcnt + __popc(pm & lt);
+            if (sidx < kRegion) region[sidx] = key;
+          }
+          wcnt += __popc(pm);
+        }
+      };
+      // Per-vector maximum in the composite order (value, first index).
+      auto vector_max_key = [&](const uint4* tile, int v, int t) -> uint64_t {
+        const uint4 q = tile[v];
+        const float vm = E::vmax(q);
+        float x[EPV];
+        E::decode(q, x);
+        int first = 0;
+        for (int e = EPV - 1; e >= 0; --e)
+          if (x[e] == vm) first = e;
+        return composite_key(vm, uint32_t(t * kTileElems + v * EPV + first));
+      };
+      // Tight speculative threshold from tile 0: each warp extracts the top L
+      // of its vector maxima, the CTA sorts the 8L candidates and takes the
+      // r-th largest (at least r elements of the tile reach it).
+      auto bootstrap_spec = [&](const uint4* tile, int nvec, int t, int r, int L) {
+        uint64_t mx[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = ctid + i * kConsumers;
+          mx[i] = v < nvec ? vector_max_key(tile, v, t) : 0ull;
+        }
+        for (int q = 0; q < L; ++q) {
+          uint64_t lm = mx[0];
+          int li = 0;
+#pragma unroll
+          for (int j = 1; j < VPT; ++j)
+            if (mx[j] > lm) {
+              lm = mx[j];
+              li = j;
+            }
+          uint64_t wm = lm;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = shfl_xor_u64(wm, o);
+            wm = y > wm ? y : wm;
+          }
+          if (lane == 0) scratch[cwarp * L + q] = wm;
+          if (wm != 0ull && lm == wm) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+              if (j == li) mx[j] = 0ull;
+          }
+        }
+        consumer_sync();
+        const int nu = kConsumerWarps * L;
+        uint64_t u = ctid < nu ? scratch[ctid] : 0ull;
+        u = block_sort_desc<kConsumers>(u, ctid, next_pow2(nu), xchg, ConsumerSync());
+        if (ctid == r - 1) S.thmin[2] = u;
+        consumer_sync();
+        const uint64_t tb = S.thmin[2];
+        if (tb > theta) theta = tb;
+        consumer_sync();  // scratch and S.thmin[2] may be reused
+      };
+      // Threshold from one tile's vector maxima: at least 8 * mw elements of
+      // the tile reach it.
+      auto bootstrap = [&](const uint4* tile, int nvec, int t, int mw) {
+        uint64_t mx[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int v = ctid + i * kConsumers;
+          mx[i] = v < nvec ? vector_max_key(tile, v, t) : 0ull;
+        }
+        const uint64_t r = warp_mth_largest<VPT>(mx, mw);
+        const uint64_t tb = cta_min(r);
+        if (tb > theta) theta = tb;
+      };
+      // Exact variant: the K-th largest vector maximum (bounds the tile's
+      // candidates by K * EPV).
+      auto bootstrap_exact = [&](const uint4* tile, int nvec, int t) {
+        for (int v = ctid; v < nvec; v += kConsumers) scratch[v] = vector_max_key(tile, v, t);
         consumer_sync();
         const uint64_t tb = block_select_kth<kConsumers>(scratch, nvec, K, ctid, S.hist, &S.sel,
                                                          ConsumerSync(), kSkip);
-        if (ctid == 0 && tb > S.theta) S.theta = tb;
-        consumer_sync();
+        if (tb > theta) theta = tb;
       };
-      // Keep exactly the K largest of the n buffered candidates; the K-th
-      // becomes the threshold.
+      // Keep exactly the K largest of the n buffered candidates.
       auto compact = [&](int n) {
         const uint64_t th = block_select_kth<kConsumers>(buf, n, K, ctid, S.hist, &S.sel,
                                                          ConsumerSync(), kSkip);
@@ -512,22 +717,18 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         }
         consumer_sync();
         for (int e = ctid; e < K; e += kConsumers) buf[e] = scratch[e];
-        if (ctid == 0) {
-          S.count = K;
-          if (th > S.theta) S.theta = th;
-        }
+        if (ctid == 0) S.count = K;
+        if (th > theta) theta = th;
         consumer_sync();
       };
 
-      for (int t = 0; t < ntiles; ++t) {
-        const uint4* tile = acquire();
-        const int nvec = tile_vectors(t);
+      // Certified handling of one tile (any address space).
+      auto certified_tile = [&](const uint4* tile, int nvec, int t) {
         const int par = int(gtile & 1u);
         const int prev = par ^ 1;
-        if (t == 0 && nvec >= K) bootstrap(tile, nvec, t);
-        uint64_t th = S.theta;
+        if (t == 0 && nvec >= K) bootstrap(tile, nvec, t, m);
         uint32_t cbits;
-        unsigned wb = phase_a(tile, nvec, composite_value(th), cbits);
+        unsigned wb = phase_a(tile, nvec, composite_value(theta), cbits);
         int bound = tally(&S.bnd[par], bnd_seen[par], wb);
         if (t > 0) {
           // insertions of the previous tile are complete once every warp passed the barrier
@@ -535,73 +736,192 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           count += int(now - ins_seen[prev]);
           ins_seen[prev] = now;
         }
-        if (count + bound > kBufCap - 8) {  // rare: make room first
+        if (count + bound > kBufCap - 8) {  // make room first
           consumer_sync();
           if (count > K) {
             compact(count);
             count = K;
           }
-          th = S.theta;
-          wb = phase_a(tile, nvec, composite_value(th), cbits);
+          wb = phase_a(tile, nvec, composite_value(theta), cbits);
           bound = tally(&S.bnd[par], bnd_seen[par], wb);
           if (count + bound > kBufCap - 8 && nvec >= K) {
-            bootstrap(tile, nvec, t);
-            th = S.theta;
-            wb = phase_a(tile, nvec, composite_value(th), cbits);
+            bootstrap_exact(tile, nvec, t);
+            wb = phase_a(tile, nvec, composite_value(theta), cbits);
             bound = tally(&S.bnd[par], bnd_seen[par], wb);
           }
         }
-        const unsigned ins = phase_b(tile, t, cbits, th);
+        const unsigned ins = phase_b(tile, t, cbits, theta);
         if (lane == 0 && ins) atomicAdd(&S.ins[par], ins);
-        release();
         ++gtile;
-      }
-      // ragged tail (fewer than 16 bytes), read directly from global memory
-      if (ctid < n_tail) {
-        const float x = E::scalar(rowp, tail_start + ctid);
-        if (x != x || x == INFINITY) {
-          bad = true;
-        } else {
-          const uint64_t key = composite_key(x, uint32_t(tail_start + ctid));
-          if (key >= S.theta) {
-            const int slot = atomicAdd(&S.count, 1);
-            if (slot < kBufCap) buf[slot] = key;
+      };
+      // Tail elements (fewer than 16 bytes), read directly from global memory.
+      auto tail_insert = [&]() {
+        if (ctid < n_tail) {
+          const float x = E::scalar(rowp, tail_start + ctid);
+          if (x != x || x == INFINITY) {
+            bad = true;
+          } else {
+            const uint64_t key = composite_key(x, uint32_t(tail_start + ctid));
+            if (key >= theta) {
+              const int slot = atomicAdd(&S.count, 1);
+              if (slot < kBufCap) buf[slot] = key;
+              else S.ovf = 1;
+            }
           }
         }
+      };
+
+      // ---- fast path: speculative threshold, one sweep
+      {
+        const int e0 = tail_start < kTileElems ? tail_start : kTileElems;  // elements in tile 0
+        const double lam = double(K) * double(e0) / double(P.V);
+        const int r = int(ceil(lam + 4.0 * sqrt(lam) + 4.0));
+        const int L = (2 * r + kConsumerWarps - 1) / kConsumerWarps;
+        for (int t = 0; t < ntiles; ++t) {
+          const uint4* tile = acquire();
+          const int nvec = tile_vectors(t);
+          if (t == 0 && L <= 32 && nvec >= kConsumerWarps * L) bootstrap_spec(tile, nvec, 0, r, L);
+          fused_pass(tile, nvec, t, theta);
+          release();
+        }
+        // tail elements go to warp 0's region
+        const bool tp_ok = ctid < n_tail;
+        uint64_t tkey = 0ull;
+        bool tpass = false;
+        if (tp_ok) {
+          const float x = E::scalar(rowp, tail_start + ctid);
+          if (x != x || x == INFINITY) {
+            bad = true;
+          } else {
+            tkey = composite_key(x, uint32_t(tail_start + ctid));
+            tpass = tkey >= theta;
+          }
+        }
+        const uint32_t pm = __ballot_sync(0xffffffffu, tpass);
+        if (cwarp == 0) {
+          if (tpass) {
+            const int sidx = wcnt + __popc(pm & ((1u << lane) - 1u));
+            if (sidx < kRegion) region[sidx] = tkey;
+          }
+          wcnt += __popc(pm);
+        }
+        if (lane == 0) S.wcnt[cwarp] = wcnt;
       }
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad, 1);
       consumer_sync();
-      count = *reinterpret_cast<volatile int*>(&S.count);
-      ins_seen[0] = *reinterpret_cast<volatile unsigned*>(&S.ins[0]);
-      ins_seen[1] = *reinterpret_cast<volatile unsigned*>(&S.ins[1]);
-      if (count > kBufCap) {  // cannot happen (capacity bound); never read past the buffer
-        if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
-        count = kBufCap;
+      {
+        int tot = 0;
+        bool ovf = false;
+        for (int i = 0; i < kConsumerWarps; ++i) {
+          tot += S.wcnt[i];
+          ovf = ovf || S.wcnt[i] > kRegion;
+        }
+        count = tot;
+        redo = S.bad == 0 && (ovf || count < K);
+      }
+      uint64_t lb = 0ull;
+      if (!redo && S.bad == 0) {
+        // certified bound over the regions: each warp's m-th largest, CTA minimum
+        uint64_t prev = ~0ull, res = 0ull;
+        for (int q = 0; q < m; ++q) {
+          uint64_t lm = 0ull;
+          for (int j = lane; j < wcnt; j += 32) {
+            const uint64_t k2 = region[j];
+            if (k2 < prev && k2 > lm) lm = k2;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const uint64_t y = shfl_xor_u64(lm, o);
+            lm = y > lm ? y : lm;
+          }
+          prev = lm;
+          res = lm;
+          if (lm == 0ull) break;
+        }
+        lb = cta_min(count > K ? res : 0ull);
+        // survivors (>= lb) of every region into scratch
+        for (int j0 = 0; j0 < wcnt; j0 += 32) {
+          const int j = j0 + lane;
+          const uint64_t k2 = j < wcnt ? region[j] : 0ull;
+          const bool keep = j < wcnt && k2 >= lb;
+          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+          int slot0 = 0;
+          if (lane == 0 && bal) slot0 = atomicAdd(&S.tmpcount, __popc(bal));
+          slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+          if (keep) {
+            const int sl = slot0 + __popc(bal & ((1u << lane) - 1u));
+            if (sl < kScratch) scratch[sl] = k2;
+          }
+        }
+        consumer_sync();
+        const int n2 = *reinterpret_cast<volatile int*>(&S.tmpcount);
+        if (n2 > kConsumers) redo = true;  // massive ties at the bound: take the exact path
+        else count = n2;
+      }
+      if (redo) {
+        // ---- certified path: the speculation missed; stream the row again
+        consumer_sync();
+        if (ctid == 0) {
+          S.count = 0;
+          S.ovf = 0;
+          S.tmpcount = 0;
+        }
+        theta = 0ull;
+        count = 0;
+        ins_seen[0] = *reinterpret_cast<volatile unsigned*>(&S.ins[0]);
+        ins_seen[1] = *reinterpret_cast<volatile unsigned*>(&S.ins[1]);
+        consumer_sync();
+        const char* rowc = static_cast<const char*>(rowp);
+        for (int t = 0; t < ntiles; ++t)
+          certified_tile(reinterpret_cast<const uint4*>(rowc + size_t(t) * kTileBytes),
+                         tile_vectors(t), t);
+        tail_insert();
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad, 1);
+        consumer_sync();
+        count = *reinterpret_cast<volatile int*>(&S.count);
+        ins_seen[0] = *reinterpret_cast<volatile unsigned*>(&S.ins[0]);
+        ins_seen[1] = *reinterpret_cast<volatile unsigned*>(&S.ins[1]);
+        if (count > kBufCap) {  // only after a data error (the path above bounds the fill)
+          if (ctid == 0 && S.bad == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
+          count = kBufCap;
+        }
+        if (count > K) compact(count);  // exact: the K largest in buf[0..K)
+        if (count > K) count = K;
+        consumer_sync();
       }
 
-      // final selection: exactly min(count, K) survivors, sorted descending
-      const int nsel = count < K ? count : K;
-      if (count > K) compact(count);  // leaves the K largest in buf[0..K)
-      const int Psz = next_pow2(nsel > 0 ? nsel : 1);
-      uint64_t v = (ctid < nsel) ? buf[ctid] : 0ull;
-      v = block_sort_desc<kConsumers>(v, ctid, Psz, xchg, ConsumerSync());
+      // final order: the survivors (scratch on the fast path, buf after the
+      // certified path) sorted descending; the first K are the top K.
+      const uint64_t* src = redo ? buf : scratch;
+      const int n = S.bad ? 0 : count;
+      const int nsel = n < K ? n : K;
+      uint64_t v = (ctid < n) ? src[ctid] : 0ull;
+      v = block_sort_desc<kConsumers>(v, ctid, next_pow2(n > 0 ? n : 1), xchg, ConsumerSync());
 
-      // temperature softmax over the survivors, top-p, renormalisation (double)
-      const bool has = ctid < nsel;
-      const float vi = composite_value(v);
-      const int idx = composite_index(v);
+      // temperature softmax over the top K, top-p, renormalisation, in double
+      // precision; the exponentials are spread over all warps (entry j on
+      // thread (j % 8) * 32 + j / 8), the prefix sums run on the sorted order.
+      double* wj = reinterpret_cast<double*>(xchg);  // free once the sort is done
+      consumer_sync();
+      if (ctid < nsel) scratch[ctid] = v;
       if (ctid == 0) {
-        S.v0 = vi;
+        S.v0 = composite_value(v);
         S.pg = 0.0;
+        S.kp = nsel;
       }
       consumer_sync();
-      const double v0 = double(S.v0);
-      const bool rowbad = S.bad != 0 || nsel == 0 || !(v0 > -INFINITY);
-      double wi = 0.0;
-      if (has && !rowbad) wi = exp((double(vi) - v0) / double(T));
-      // inclusive scan of wi over the first nsel threads (warps beyond hold 0)
-      double incl = wi;
-      const bool active_warp = cwarp * 32 < Psz;
+      const float v0f = S.v0;
+      const bool rowbad = S.bad != 0 || nsel == 0 || !(v0f > -INFINITY);
+      {
+        const int j = (ctid % 32) * kConsumerWarps + cwarp;  // strided over the warps
+        if (j < nsel && !rowbad)
+          wj[j] = exp((double(composite_value(scratch[j])) - double(v0f)) / double(T));
+      }
+      consumer_sync();
+      const bool act = ctid < nsel && !rowbad;
+      const double wv = act ? wj[ctid] : 0.0;
+      double incl = wv;
+      const bool active_warp = cwarp * 32 < nsel;
       if (active_warp) {
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -612,27 +932,24 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       }
       consumer_sync();
       double woff = 0.0, W = 0.0;
-      if (active_warp) {
-        for (int i = 0; i < kConsumerWarps && i * 32 < Psz; ++i) {
+      if (active_warp)
+        for (int i = 0; i < kConsumerWarps && i * 32 < nsel; ++i) {
           if (i < cwarp) woff += S.red_d[i];
           W += S.red_d[i];
         }
-      }
       incl += woff;
-      const double before = incl - wi;
-      const bool keep = has && (tp >= 1.0f || before / W < double(tp));
-      // the kept set is the prefix that ends at the first dropped survivor
-      const uint32_t drop = __ballot_sync(0xffffffffu, has && !keep);
-      if (lane == 0) S.red_i[cwarp] = drop ? cwarp * 32 + __ffs(drop) - 1 : INT_MAX;
+      // the kept set is the prefix that ends at the first token whose
+      // cumulative probability before it is not below top_p
+      if (tp < 1.0f && act && !((incl - wv) / W < double(tp))) atomicMin(&S.kp, ctid);
       consumer_sync();
-      int kp = nsel;
-      for (int i = 0; i < kConsumerWarps; ++i) kp = S.red_i[i] < kp ? S.red_i[i] : kp;
+      const int kp = S.kp;
       if (ctid == kp - 1) S.wp = incl;
       consumer_sync();
       const double Wp = S.wp;
       const size_t cbase = size_t(row) * kTopkMax;
-      if (ctid < kp && !rowbad) {
-        const double p = wi / Wp;
+      if (act && ctid < kp) {
+        const int idx = composite_index(v);
+        const double p = wv / Wp;
         w.cand_idx[cbase + ctid] = idx;
         w.cand_p[cbase + ctid] = p;
         if (idx == gx) S.pg = p;
@@ -643,14 +960,15 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         RowStat st;
         st.s = Wp;
         st.pg = gx >= 0 ? S.pg : __longlong_as_double(0x7ff8000000000000LL);
-        st.m = S.v0;
+        st.m = v0f;
         st.arg = -1;
         st.kept = rowbad ? 0 : kp;
         st.mode = kTopk;
         w.stats[row] = st;
         S.count = 0;
-        S.theta = 0ull;
         S.bad = 0;
+        S.ovf = 0;
+        S.tmpcount = 0;
       }
     }
 

@@ -135,6 +135,38 @@ __device__ uint64_t block_sort_desc(uint64_t v, int tid, int P, uint64_t* xchg, 
   return v;
 }
 
+// Warp-level: the m-th largest of the nonzero keys the lanes hold (NV per
+// lane, 0 = empty slot, keys unique), by m rounds of warp max with removal.
+// Returns 0 when the warp holds fewer than m keys.  Warp-uniform result.
+template <int NV>
+__device__ __forceinline__ uint64_t warp_mth_largest(uint64_t (&k)[NV], int m) {
+  uint64_t res = 0ull;
+  for (int r = 0; r < m; ++r) {
+    uint64_t lm = k[0];
+    int li = 0;
+#pragma unroll
+    for (int j = 1; j < NV; ++j)
+      if (k[j] > lm) {
+        lm = k[j];
+        li = j;
+      }
+    uint64_t wm = lm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t y = shfl_xor_u64(wm, o);
+      wm = y > wm ? y : wm;
+    }
+    res = wm;
+    if (wm == 0ull) break;
+    if (lm == wm) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j)
+        if (j == li) k[j] = 0ull;
+    }
+  }
+  return res;
+}
+
 __host__ __device__ __forceinline__ int next_pow2(int n) {
   int p = 1;
   while (p < n) p <<= 1;
