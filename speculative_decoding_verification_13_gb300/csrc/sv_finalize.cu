@@ -235,6 +235,201 @@ __device__ int unfiltered_draw(const void* trow, const void* drow, int V, Weight
   return S.ystar;
 }
 
+// Per-warp scratch for selecting one filtered row's top k.
+struct WarpSel {
+  int hist[256];
+  uint64_t list[kTopkMax];  // the row's top k, then sorted descending
+  double w[kTopkMax];       // exp((x_j - x_max) / T) in sorted order
+  double before[kTopkMax];  // sum of the weights before j (sorted order)
+  int digit, above, cnt, pad;
+};
+
+// Exact k-th largest of the n (> k) unique keys at keys[] (any memory), by
+// MSB-first radix selection over 8-bit digits with a warp-private histogram;
+// stops once the remaining prefix group is selected whole.
+__device__ uint64_t warp_select_kth(const uint64_t* keys, int n, int k, WarpSel& ws,
+                                    uint32_t skip) {
+  const int lane = threadIdx.x & 31;
+  uint64_t prefix = 0ull, mask = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    if ((skip >> (shift / 8)) & 1u) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ws.hist[lane * 8 + j] = 0;
+    __syncwarp();
+    for (int base = 0; base < n; base += 32) {
+      const int e = base + lane;
+      bool valid = false;
+      uint32_t d = 0;
+      if (e < n) {
+        const uint64_t key = keys[e];
+        if ((key & mask) == prefix) {
+          valid = true;
+          d = uint32_t(key >> shift) & 255u;
+        }
+      }
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t peers = __match_any_sync(vm, d);
+        if (lane == __ffs(peers) - 1) ws.hist[d] += __popc(peers);  // distinct digits per step
+      }
+      __syncwarp();
+    }
+    int cnt[8], loc = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      cnt[j] = ws.hist[lane * 8 + j];
+      loc += cnt[j];
+    }
+    int suf = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
+    }
+    int acc = suf - loc;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (acc < need && acc + cnt[j] >= need) {
+        ws.digit = lane * 8 + j;
+        ws.above = acc;
+        ws.cnt = cnt[j];
+      }
+      acc += cnt[j];
+    }
+    __syncwarp();
+    const int d = ws.digit;
+    need -= ws.above;
+    const int grp = ws.cnt;
+    __syncwarp();
+    prefix |= uint64_t(d) << shift;
+    mask |= 255ull << shift;
+    if (grp == need) {
+      uint64_t mn = ~0ull;
+      for (int e = lane; e < n; e += 32) {
+        const uint64_t key = keys[e];
+        if ((key & mask) == prefix && key < mn) mn = key;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t y = shfl_xor_u64(mn, o);
+        mn = y < mn ? y : mn;
+      }
+      return mn;
+    }
+  }
+  return prefix;
+}
+
+// Bitonic sort, descending, of a[0..P) in shared memory by one warp (P a power of two).
+__device__ void warp_sort_desc(uint64_t* a, int P) {
+  const int lane = threadIdx.x & 31;
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int p = lane; p < P / 2; p += 32) {
+        const int i = (p / j) * 2 * j + (p % j);  // lower index of the pair
+        const int q = i + j;
+        const uint64_t x = a[i], y = a[q];
+        const bool desc = (i & size) == 0;
+        if (desc ? (x < y) : (x > y)) {
+          a[i] = y;
+          a[q] = x;
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// One filtered row: exact top k of the row pass's survivors (composite order:
+// logit descending, index ascending), then the temperature softmax over them,
+// the top-p cut (keep j while the probability mass before j is below top_p)
+// and the renormalisation, in double precision.  Writes the kept list, the
+// kept size and p(x) of the row's draft token.  One warp.
+template <bool BF16>
+__device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float tp, int gx,
+                                WarpSel& ws) {
+  const Ws& w = P.ws;
+  const int lane = threadIdx.x & 31;
+  const uint32_t lt = (1u << lane) - 1u;
+  const int n = w.stats[row].kept;
+  const uint64_t* raw = w.cand_raw + size_t(row) * kRawCap;
+  const uint64_t th = n > K ? warp_select_kth(raw, n, K, ws, BF16 ? kSkipBf16 : kSkipF32) : 0ull;
+  int cnt = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int e = base + lane;
+    const uint64_t key = e < n ? raw[e] : 0ull;
+    const bool keep = e < n && key >= th;
+    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int sl = cnt + __popc(bal & lt);
+      if (sl < kTopkMax) ws.list[sl] = key;
+    }
+    cnt += __popc(bal);
+  }
+  const int nsel = cnt < K ? cnt : K;
+  const int Psz = next_pow2(nsel > 0 ? nsel : 1);
+  for (int j = nsel + lane; j < Psz; j += 32) ws.list[j] = 0ull;
+  __syncwarp();
+  warp_sort_desc(ws.list, Psz);
+  const double v0 = double(composite_value(ws.list[0]));
+  double carry = 0.0;
+  for (int j0 = 0; j0 < nsel; j0 += 32) {
+    const int j = j0 + lane;
+    const double wv = j < nsel ? exp((double(composite_value(ws.list[j])) - v0) / double(T)) : 0.0;
+    double incl = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (j < nsel) {
+      ws.w[j] = wv;
+      ws.before[j] = carry + incl - wv;
+    }
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  const double W = carry;
+  int kp = nsel;
+  if (tp < 1.0f) {
+    for (int j0 = 0; j0 < nsel && kp == nsel; j0 += 32) {
+      const int j = j0 + lane;
+      const bool drop = j < nsel && !(ws.before[j] < double(tp) * W);
+      const uint32_t bal = __ballot_sync(0xffffffffu, drop);
+      if (bal) kp = j0 + __ffs(bal) - 1;
+    }
+  }
+  const double Wp = kp < nsel ? ws.before[kp] : W;
+  const double inv = 1.0 / Wp;
+  const size_t cbase = size_t(row) * kTopkMax;
+  bool hit = false;
+  double pgv = 0.0;
+  for (int j = lane; j < kp; j += 32) {
+    const int idx = composite_index(ws.list[j]);
+    const double pj = ws.w[j] * inv;
+    w.cand_idx[cbase + j] = idx;
+    w.cand_p[cbase + j] = pj;
+    if (idx == gx) {
+      hit = true;
+      pgv = pj;
+    }
+  }
+  const uint32_t hb = __ballot_sync(0xffffffffu, hit);
+  if (hb) pgv = __shfl_sync(0xffffffffu, pgv, __ffs(hb) - 1);
+  if (lane == 0) {
+    RowStat st;
+    st.s = Wp;
+    st.pg = gx >= 0 ? pgv : __longlong_as_double(0x7ff8000000000000LL);
+    st.m = float(v0);
+    st.arg = -1;
+    st.kept = kp;
+    st.mode = kTopk;
+    w.stats[row] = st;
+  }
+  __syncwarp();
+}
+
 // Inverse-CDF draw over kept sets (double, index order).  All threads call.
 //   residual: target kept set of row tr against draft kept set of row dr
 //   bonus   : target kept set of row tr
@@ -300,7 +495,9 @@ __device__ int filtered_draw(const Problem& P, int64_t tr, int64_t dr, bool resi
 
 template <bool BF16>
 __global__ void __launch_bounds__(kFinalThreads) finalize_kernel(const Problem P) {
-  extern __shared__ float tile_sum[];
+  extern __shared__ __align__(16) unsigned char fsmem[];
+  WarpSel* wsel = reinterpret_cast<WarpSel*>(fsmem);
+  float* tile_sum = reinterpret_cast<float*>(fsmem + sizeof(WarpSel) * kWarps);
   __shared__ FinalShared S;
   const Ws& w = P.ws;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -328,6 +525,26 @@ __global__ void __launch_bounds__(kFinalThreads) finalize_kernel(const Problem P
   }
   const float T = P.temperature[b];
   const bool greedy = T == 0.0f;
+
+  // Filtered requests: exact top k, softmax and top-p of every row (target
+  // rows 0..k, draft rows 0..k-1), one warp per row.
+  if (!greedy && w.stats[t0].mode == kTopk) {
+    const int K = P.top_k[b];
+    const float tp = P.top_p ? P.top_p[b] : 1.0f;
+    for (int i = warp; i < 2 * k + 1; i += kWarps) {
+      int64_t row;
+      int gx;
+      if (i <= k) {
+        row = t0 + i;
+        gx = i < k ? P.draft_tokens[d0 + i] : -1;
+      } else {
+        row = P.Rt + d0 + (i - k - 1);
+        gx = P.draft_tokens[d0 + (i - k - 1)];
+      }
+      warp_filter_row<BF16>(P, row, K, T, tp, gx, wsel[warp]);
+    }
+    __syncthreads();
+  }
 
   if (warp == 0) {
     bool acc = false;
@@ -397,7 +614,7 @@ __global__ void __launch_bounds__(kFinalThreads) finalize_kernel(const Problem P
 }  // namespace
 
 size_t finalize_smem_bytes(int V) {
-  return sizeof(float) * size_t((V + kScanTile - 1) / kScanTile);
+  return sizeof(WarpSel) * kWarps + sizeof(float) * size_t((V + kScanTile - 1) / kScanTile);
 }
 
 cudaError_t launch_finalize(const Problem& P, bool bf16, cudaStream_t s) {

@@ -20,6 +20,7 @@ constexpr int kTileBytes = 16384;                        // one bulk copy
 constexpr int kStages = 4;                               // smem ring depth per CTA
 constexpr int kBufCap = 2560;                            // top-k candidate buffer
 constexpr int kRegion = kBufCap / kConsumerWarps;        // per-warp region (fast path)
+constexpr int kRawCap = 1024;                            // top-k survivors kept per row
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr int kFinalThreads = 256;
@@ -41,11 +42,11 @@ struct WsHeader {
 };
 
 struct RowStat {
-  double s;     // softmax normaliser (unfiltered sampling rows)
+  double s;     // softmax normaliser (sampling rows; kept-set weight for filtered rows)
   double pg;    // p(x) of the row's draft token
   float m;      // row max logit
   int32_t arg;  // greedy argmax
-  int32_t kept; // kept-set size (filtered rows)
+  int32_t kept; // filtered rows: survivors after the row pass, then the kept-set size
   int32_t mode;
 };
 
@@ -57,10 +58,11 @@ struct Ws {
   RowStat* stats;    // [R]
   int32_t* cand_idx; // [R, kTopkMax]
   double* cand_p;    // [R, kTopkMax]
+  uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys)
 };
 
 struct WsLayout {
-  size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, total;
+  size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, off_raw, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -75,6 +77,7 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   L.off_stats = o;   o = align256(o + sizeof(RowStat) * (size_t)(R > 0 ? R : 1));
   L.off_cidx = o;    o = align256(o + sizeof(int32_t) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_cp = o;      o = align256(o + sizeof(double) * kTopkMax * (size_t)(R > 0 ? R : 1));
+  L.off_raw = o;     o = align256(o + sizeof(uint64_t) * kRawCap * (size_t)(R > 0 ? R : 1));
   L.total = o;
   return L;
 }
@@ -89,6 +92,7 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.stats = reinterpret_cast<RowStat*>(p + L.off_stats);
   w.cand_idx = reinterpret_cast<int32_t*>(p + L.off_cidx);
   w.cand_p = reinterpret_cast<double*>(p + L.off_cp);
+  w.cand_raw = reinterpret_cast<uint64_t*>(p + L.off_raw);
   return w;
 }
 

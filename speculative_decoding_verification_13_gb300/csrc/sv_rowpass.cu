@@ -53,8 +53,10 @@ struct RowShared {
   int bad;
   int kp;
   int wcnt[kConsumerWarps];
+  uint16_t queue[kConsumerWarps][(kTileBytes / 16 + kConsumers - 1) / kConsumers * 32];
   float v0;
   double wp;
+  double inv_wp;
   double pg;
   float red_f[kConsumerWarps];
   int red_i[kConsumerWarps];
@@ -570,41 +572,47 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       int wcnt = 0;  // fill of this warp's region (warp-uniform)
       auto fused_pass = [&](const uint4* tile, int nvec, int t, uint64_t th) {
         const float thv = composite_value(th);
-        uint32_t mk[VPT];
-        int total = 0;
+        const uint32_t lt = (1u << lane) - 1u;
+        uint16_t* queue = S.queue[cwarp];
+        int qn = 0;  // flagged vectors of this warp in this tile (warp-uniform)
+        if (nvec == kTileBytes / 16) {
+          // full tile: two vectors per compare, no bounds checks
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int v0 = ctid + i * kConsumers;
-          const bool c = v0 < nvec && !(E::vmax(tile[v0]) < thv);
-          mk[i] = __ballot_sync(0xffffffffu, c);
-          total += __popc(mk[i]);
+          for (int i = 0; i < VPT; i += 2) {
+            const int va = ctid + i * kConsumers, vb = va + kConsumers;
+            const uint4 qa = tile[va], qb = tile[vb];
+            const bool any = !(fmax_nan(E::vmax(qa), E::vmax(qb)) < thv);
+            if (__any_sync(0xffffffffu, any)) {
+              const bool ca = any && !(E::vmax(qa) < thv);
+              const bool cb = any && !(E::vmax(qb) < thv);
+              const uint32_t ba = __ballot_sync(0xffffffffu, ca);
+              if (ca) queue[qn + __popc(ba & lt)] = uint16_t(va);
+              qn += __popc(ba);
+              const uint32_t bb = __ballot_sync(0xffffffffu, cb);
+              if (cb) queue[qn + __popc(bb & lt)] = uint16_t(vb);
+              qn += __popc(bb);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < VPT; ++i) {
+            const int v0 = ctid + i * kConsumers;
+            const bool c = v0 < nvec && !(E::vmax(tile[v0]) < thv);
+            const uint32_t bal = __ballot_sync(0xffffffffu, c);
+            if (c) queue[qn + __popc(bal & lt)] = uint16_t(v0);
+            qn += __popc(bal);
+          }
         }
-        if (total == 0) return;
+        if (qn == 0) return;
+        __syncwarp();
         const int g = lane / EPV, e = lane % EPV;
         const char* tb = reinterpret_cast<const char*>(tile);
-        const uint32_t lt = (1u << lane) - 1u;
-        for (int b0 = 0; b0 < total; b0 += GROUP) {
-          int n = b0 + g;
+        for (int b0 = 0; b0 < qn; b0 += GROUP) {
+          const int n = b0 + g;
           uint64_t key = 0ull;
           bool pass = false;
-          if (n < total) {
-            int slot = 0;
-            uint32_t bits = mk[0];
-            bool found = false;
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-              const int c = __popc(mk[i]);
-              if (!found) {
-                if (n < c) {
-                  found = true;
-                  slot = i;
-                  bits = mk[i];
-                } else {
-                  n -= c;
-                }
-              }
-            }
-            const int v = cwarp * 32 + nth_set_bit(bits, n) + slot * kConsumers;
+          if (n < qn) {
+            const int v = queue[n];
             const float x = element(tb, v, e);
             if (x != x || x == INFINITY) {
               bad = true;
@@ -620,6 +628,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           }
           wcnt += __popc(pm);
         }
+        __syncwarp();  // the queue is rewritten by the next tile
       };
       // Per-vector maximum in the composite order (value, first index).
       auto vector_max_key = [&](const uint4* tile, int v, int t) -> uint64_t {
@@ -634,13 +643,16 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       };
       // Tight speculative threshold from tile 0: each warp extracts the top L
       // of its vector maxima, the CTA sorts the 8L candidates and takes the
-      // r-th largest (at least r elements of the tile reach it).
+      // r-th largest.  A speculative threshold needs no exact tie order (the
+      // row-end check decides), so a vector maximum is keyed with the index
+      // of the vector's first element.
       auto bootstrap_spec = [&](const uint4* tile, int nvec, int t, int r, int L) {
         uint64_t mx[VPT];
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
           const int v = ctid + i * kConsumers;
-          mx[i] = v < nvec ? vector_max_key(tile, v, t) : 0ull;
+          mx[i] = v < nvec ? composite_key(E::vmax(tile[v]), uint32_t(t * kTileElems + v * EPV))
+                           : 0ull;
         }
         for (int q = 0; q < L; ++q) {
           uint64_t lm = mx[0];
@@ -819,45 +831,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         count = tot;
         redo = S.bad == 0 && (ovf || count < K);
       }
-      uint64_t lb = 0ull;
-      if (!redo && S.bad == 0) {
-        // certified bound over the regions: each warp's m-th largest, CTA minimum
-        uint64_t prev = ~0ull, res = 0ull;
-        for (int q = 0; q < m; ++q) {
-          uint64_t lm = 0ull;
-          for (int j = lane; j < wcnt; j += 32) {
-            const uint64_t k2 = region[j];
-            if (k2 < prev && k2 > lm) lm = k2;
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const uint64_t y = shfl_xor_u64(lm, o);
-            lm = y > lm ? y : lm;
-          }
-          prev = lm;
-          res = lm;
-          if (lm == 0ull) break;
-        }
-        lb = cta_min(count > K ? res : 0ull);
-        // survivors (>= lb) of every region into scratch
-        for (int j0 = 0; j0 < wcnt; j0 += 32) {
-          const int j = j0 + lane;
-          const uint64_t k2 = j < wcnt ? region[j] : 0ull;
-          const bool keep = j < wcnt && k2 >= lb;
-          const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-          int slot0 = 0;
-          if (lane == 0 && bal) slot0 = atomicAdd(&S.tmpcount, __popc(bal));
-          slot0 = __shfl_sync(0xffffffffu, slot0, 0);
-          if (keep) {
-            const int sl = slot0 + __popc(bal & ((1u << lane) - 1u));
-            if (sl < kScratch) scratch[sl] = k2;
-          }
-        }
-        consumer_sync();
-        const int n2 = *reinterpret_cast<volatile int*>(&S.tmpcount);
-        if (n2 > kConsumers) redo = true;  // massive ties at the bound: take the exact path
-        else count = n2;
-      }
+      if (!redo && S.bad == 0 && count > kRawCap) redo = true;  // too many survivors: exact path
       if (redo) {
         // ---- certified path: the speculation missed; stream the row again
         consumer_sync();
@@ -890,79 +864,28 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         consumer_sync();
       }
 
-      // final order: the survivors (scratch on the fast path, buf after the
-      // certified path) sorted descending; the first K are the top K.
-      const uint64_t* src = redo ? buf : scratch;
-      const int n = S.bad ? 0 : count;
-      const int nsel = n < K ? n : K;
-      uint64_t v = (ctid < n) ? src[ctid] : 0ull;
-      v = block_sort_desc<kConsumers>(v, ctid, next_pow2(n > 0 ? n : 1), xchg, ConsumerSync());
-
-      // temperature softmax over the top K, top-p, renormalisation, in double
-      // precision; the exponentials are spread over all warps (entry j on
-      // thread (j % 8) * 32 + j / 8), the prefix sums run on the sorted order.
-      double* wj = reinterpret_cast<double*>(xchg);  // free once the sort is done
-      consumer_sync();
-      if (ctid < nsel) scratch[ctid] = v;
-      if (ctid == 0) {
-        S.v0 = composite_value(v);
-        S.pg = 0.0;
-        S.kp = nsel;
-      }
-      consumer_sync();
-      const float v0f = S.v0;
-      const bool rowbad = S.bad != 0 || nsel == 0 || !(v0f > -INFINITY);
-      {
-        const int j = (ctid % 32) * kConsumerWarps + cwarp;  // strided over the warps
-        if (j < nsel && !rowbad)
-          wj[j] = exp((double(composite_value(scratch[j])) - double(v0f)) / double(T));
-      }
-      consumer_sync();
-      const bool act = ctid < nsel && !rowbad;
-      const double wv = act ? wj[ctid] : 0.0;
-      double incl = wv;
-      const bool active_warp = cwarp * 32 < nsel;
-      if (active_warp) {
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+      // publish the survivors: the per-warp regions (fast path) or buf[0..K)
+      // (certified path), contiguously; the finalize kernel selects the exact
+      // top K from them and applies the temperature softmax and top-p.
+      const size_t rbase = size_t(row) * kRawCap;
+      if (S.bad == 0) {
+        if (redo) {
+          for (int j = ctid; j < count; j += kConsumers) w.cand_raw[rbase + j] = buf[j];
+        } else {
+          int off = 0;
+          for (int i = 0; i < cwarp; ++i) off += S.wcnt[i];
+          for (int j = lane; j < wcnt; j += 32) w.cand_raw[rbase + off + j] = region[j];
         }
-        if (lane == 31) S.red_d[cwarp] = incl;
-      }
-      consumer_sync();
-      double woff = 0.0, W = 0.0;
-      if (active_warp)
-        for (int i = 0; i < kConsumerWarps && i * 32 < nsel; ++i) {
-          if (i < cwarp) woff += S.red_d[i];
-          W += S.red_d[i];
-        }
-      incl += woff;
-      // the kept set is the prefix that ends at the first token whose
-      // cumulative probability before it is not below top_p
-      if (tp < 1.0f && act && !((incl - wv) / W < double(tp))) atomicMin(&S.kp, ctid);
-      consumer_sync();
-      const int kp = S.kp;
-      if (ctid == kp - 1) S.wp = incl;
-      consumer_sync();
-      const double Wp = S.wp;
-      const size_t cbase = size_t(row) * kTopkMax;
-      if (act && ctid < kp) {
-        const int idx = composite_index(v);
-        const double p = wv / Wp;
-        w.cand_idx[cbase + ctid] = idx;
-        w.cand_p[cbase + ctid] = p;
-        if (idx == gx) S.pg = p;
       }
       consumer_sync();
       if (ctid == 0) {
-        if (rowbad) flag_request(w, b, SV_ERR_DATA_LOGIT, row);
+        if (S.bad) flag_request(w, b, SV_ERR_DATA_LOGIT, row);
         RowStat st;
-        st.s = Wp;
-        st.pg = gx >= 0 ? S.pg : __longlong_as_double(0x7ff8000000000000LL);
-        st.m = v0f;
+        st.s = 0.0;
+        st.pg = __longlong_as_double(0x7ff8000000000000LL);
+        st.m = 0.0f;
         st.arg = -1;
-        st.kept = rowbad ? 0 : kp;
+        st.kept = S.bad ? 0 : count;
         st.mode = kTopk;
         w.stats[row] = st;
         S.count = 0;
