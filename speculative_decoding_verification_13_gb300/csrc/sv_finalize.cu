@@ -22,6 +22,7 @@ namespace sv {
 namespace {
 
 constexpr int kWarps = kFinalThreads / 32;
+static_assert(kFinalThreads >= kTopkMax, "one thread per kept token in the filtered draw");
 constexpr int kScanTile = 256;  // elements per warp tile (32 lanes x 8)
 
 struct BlockSync {
@@ -240,9 +241,10 @@ struct WarpSel {
   int hist[256];
   uint64_t list[kTopkMax];  // the row's top k, then sorted descending
   double w[kTopkMax];       // exp((x_j - x_max) / T) in sorted order
-  double before[kTopkMax];  // sum of the weights before j (sorted order)
   int digit, above, cnt, pad;
 };
+
+constexpr int kRegKeys = 10;  // survivors held in registers per lane (320 per warp)
 
 // Exact k-th largest of the n (> k) unique keys at keys[] (any memory), by
 // MSB-first radix selection over 8-bit digits with a warp-private histogram;
@@ -321,6 +323,78 @@ __device__ uint64_t warp_select_kth(const uint64_t* keys, int n, int k, WarpSel&
   return prefix;
 }
 
+// Same selection over keys held in registers (lane holds keys[j] = key
+// j * 32 + lane, 0 for an empty slot).
+__device__ uint64_t warp_select_kth_regs(const uint64_t (&keys)[kRegKeys], int k, WarpSel& ws,
+                                         uint32_t skip) {
+  const int lane = threadIdx.x & 31;
+  uint64_t prefix = 0ull, mask = 0ull;
+  int need = k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    if ((skip >> (shift / 8)) & 1u) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ws.hist[lane * 8 + j] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < kRegKeys; ++r) {
+      const uint64_t key = keys[r];
+      const bool valid = key != 0ull && (key & mask) == prefix;
+      const uint32_t d = uint32_t(key >> shift) & 255u;
+      const uint32_t vm = __ballot_sync(0xffffffffu, valid);
+      if (vm == 0u) continue;
+      if (valid) {
+        const uint32_t peers = __match_any_sync(vm, d);
+        if (lane == __ffs(peers) - 1) ws.hist[d] += __popc(peers);
+      }
+      __syncwarp();
+    }
+    int cnt[8], loc = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      cnt[j] = ws.hist[lane * 8 + j];
+      loc += cnt[j];
+    }
+    int suf = loc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_down_sync(0xffffffffu, suf, o);
+      if (lane + o < 32) suf += y;
+    }
+    int acc = suf - loc;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (acc < need && acc + cnt[j] >= need) {
+        ws.digit = lane * 8 + j;
+        ws.above = acc;
+        ws.cnt = cnt[j];
+      }
+      acc += cnt[j];
+    }
+    __syncwarp();
+    const int d = ws.digit;
+    need -= ws.above;
+    const int grp = ws.cnt;
+    __syncwarp();
+    prefix |= uint64_t(d) << shift;
+    mask |= 255ull << shift;
+    if (grp == need) {
+      uint64_t mn = ~0ull;
+#pragma unroll
+      for (int r = 0; r < kRegKeys; ++r) {
+        const uint64_t key = keys[r];
+        if (key != 0ull && (key & mask) == prefix && key < mn) mn = key;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t y = shfl_xor_u64(mn, o);
+        mn = y < mn ? y : mn;
+      }
+      return mn;
+    }
+  }
+  return prefix;
+}
+
 // Bitonic sort, descending, of a[0..P) in shared memory by one warp (P a power of two).
 __device__ void warp_sort_desc(uint64_t* a, int P) {
   const int lane = threadIdx.x & 31;
@@ -354,18 +428,39 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
   const uint32_t lt = (1u << lane) - 1u;
   const int n = w.stats[row].kept;
   const uint64_t* raw = w.cand_raw + size_t(row) * kRawCap;
-  const uint64_t th = n > K ? warp_select_kth(raw, n, K, ws, BF16 ? kSkipBf16 : kSkipF32) : 0ull;
+  const uint32_t skip = BF16 ? kSkipBf16 : kSkipF32;
   int cnt = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int e = base + lane;
-    const uint64_t key = e < n ? raw[e] : 0ull;
-    const bool keep = e < n && key >= th;
-    const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int sl = cnt + __popc(bal & lt);
-      if (sl < kTopkMax) ws.list[sl] = key;
+  if (n <= 32 * kRegKeys) {
+    uint64_t keys[kRegKeys];
+#pragma unroll
+    for (int r = 0; r < kRegKeys; ++r) {
+      const int e = r * 32 + lane;
+      keys[r] = e < n ? raw[e] : 0ull;
     }
-    cnt += __popc(bal);
+    const uint64_t th = n > K ? warp_select_kth_regs(keys, K, ws, skip) : 0ull;
+#pragma unroll
+    for (int r = 0; r < kRegKeys; ++r) {
+      const bool keep = keys[r] != 0ull && keys[r] >= th;
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int sl = cnt + __popc(bal & lt);
+        if (sl < kTopkMax) ws.list[sl] = keys[r];
+      }
+      cnt += __popc(bal);
+    }
+  } else {
+    const uint64_t th = n > K ? warp_select_kth(raw, n, K, ws, skip) : 0ull;
+    for (int base = 0; base < n; base += 32) {
+      const int e = base + lane;
+      const uint64_t key = e < n ? raw[e] : 0ull;
+      const bool keep = e < n && key >= th;
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
+        const int sl = cnt + __popc(bal & lt);
+        if (sl < kTopkMax) ws.list[sl] = key;
+      }
+      cnt += __popc(bal);
+    }
   }
   const int nsel = cnt < K ? cnt : K;
   const int Psz = next_pow2(nsel > 0 ? nsel : 1);
@@ -373,34 +468,57 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
   __syncwarp();
   warp_sort_desc(ws.list, Psz);
   const double v0 = double(composite_value(ws.list[0]));
-  double carry = 0.0;
+  const double invT = 1.0 / double(T);
+  // Weights w_j = exp((x_j - x_max) / T) in double (w_0 = 1, all in (0, 1]).
+  // Their prefix sums are taken exactly in 64-bit fixed point (unit 2^-55;
+  // at most K * 2^-56 absolute rounding), which keeps FP64 work, the scarce
+  // resource here, to one exponential and two multiplies per token.
+  constexpr double kFix = 36028797018963968.0;  // 2^55: K <= 256 weights <= 1 sum below 2^63
+  unsigned long long carry = 0ull;
   for (int j0 = 0; j0 < nsel; j0 += 32) {
     const int j = j0 + lane;
-    const double wv = j < nsel ? exp((double(composite_value(ws.list[j])) - v0) / double(T)) : 0.0;
-    double incl = wv;
+    double wv = 0.0;
+    if (j < nsel) {
+      wv = exp((double(composite_value(ws.list[j])) - v0) * invT);
+      ws.w[j] = wv;
+    }
+    unsigned long long incl = (unsigned long long)__double2ull_rn(wv * kFix);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
-    }
-    if (j < nsel) {
-      ws.w[j] = wv;
-      ws.before[j] = carry + incl - wv;
     }
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   __syncwarp();
-  const double W = carry;
+  const unsigned long long Wfx = carry;
+  // the kept prefix ends at the first j whose mass before it is not below top_p
   int kp = nsel;
+  unsigned long long Wpfx = Wfx;
   if (tp < 1.0f) {
+    const double lim = double(tp) * double(Wfx);
+    unsigned long long c2 = 0ull;
     for (int j0 = 0; j0 < nsel && kp == nsel; j0 += 32) {
       const int j = j0 + lane;
-      const bool drop = j < nsel && !(ws.before[j] < double(tp) * W);
+      const unsigned long long mine =
+          j < nsel ? (unsigned long long)__double2ull_rn(ws.w[j] * kFix) : 0ull;
+      unsigned long long incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned long long before = c2 + incl - mine;
+      const bool drop = j < nsel && !(double(before) < lim);
       const uint32_t bal = __ballot_sync(0xffffffffu, drop);
-      if (bal) kp = j0 + __ffs(bal) - 1;
+      if (bal) {
+        kp = j0 + __ffs(bal) - 1;
+        Wpfx = __shfl_sync(0xffffffffu, before, kp - j0);
+      }
+      c2 += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  const double Wp = kp < nsel ? ws.before[kp] : W;
+  const double Wp = double(Wpfx) / kFix;
   const double inv = 1.0 / Wp;
   const size_t cbase = size_t(row) * kTopkMax;
   bool hit = false;
@@ -494,7 +612,7 @@ __device__ int filtered_draw(const Problem& P, int64_t tr, int64_t dr, bool resi
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kFinalThreads) finalize_kernel(const Problem P) {
+__global__ void __launch_bounds__(kFinalThreads, 1) finalize_kernel(const Problem P) {
   extern __shared__ __align__(16) unsigned char fsmem[];
   WarpSel* wsel = reinterpret_cast<WarpSel*>(fsmem);
   float* tile_sum = reinterpret_cast<float*>(fsmem + sizeof(WarpSel) * kWarps);

@@ -23,7 +23,7 @@ constexpr int kRegion = kBufCap / kConsumerWarps;        // per-warp region (fas
 constexpr int kRawCap = 1024;                            // top-k survivors kept per row
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
-constexpr int kFinalThreads = 256;
+constexpr int kFinalThreads = 512;
 constexpr int kFinalTileElems = kFinalThreads * 8;       // elements per scan tile
 constexpr int kMaxFinalTiles = (SV_VOCAB_MAX + kFinalTileElems - 1) / kFinalTileElems;
 constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
