@@ -160,6 +160,39 @@ int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t
                           double* stats, int32_t* kept_count, int32_t* kept_idx,
                           double* kept_p);
 
+/* ---- allocation-free variant ----------------------------------------------
+ * The pages describe no counterpart of this entry point: it is a convenience of
+ * this library for callers that cannot allocate device memory where they
+ * verify (a C host program that links only this library and owns no device
+ * allocator; a serving loop whose device memory is planned once and which must
+ * not allocate inside its decode step).
+ *
+ * spec_verify_noalloc computes exactly what spec_verify computes, with the
+ * same arguments minus the workspace: the workspace is a fixed buffer of
+ * SV_NOALLOC_SCRATCH_BYTES inside the library (one per device).
+ *   - A batch whose spec_verify_workspace_size exceeds SV_NOALLOC_SCRATCH_BYTES
+ *     returns SV_ERR_WORKSPACE before anything is enqueued (16 MiB holds about
+ *     1,400 logit rows, e.g. 32 requests with k = 15).
+ *   - The buffer is shared: calls that can overlap on one device race on it.
+ *     Order them on one stream or with events.
+ *   - The buffer's address is looked up once per device, with that device
+ *     current, on the first call; make that first call before any stream
+ *     capture begins.
+ *   - Nothing in the buffer has to start at zero.
+ * Returns SV_OK once the work is enqueued, else an SV_ERR_* code. */
+#define SV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+int spec_verify_noalloc(const sv_logits* target_logits, const sv_logits* draft_logits,
+                        const int32_t* draft_tokens, const int32_t* k_per_req,
+                        const float* temperature, const int32_t* top_k, const float* top_p,
+                        const float* uniforms, int32_t* out_accept_len, int32_t* out_tokens,
+                        void* stream, int32_t batch, const sv_options* options);
+
+/* Device address and size of the current device's spec_verify_noalloc buffer,
+ * so that spec_verify_get_error / spec_verify_dump_rows can read the last
+ * allocation-free call. */
+int spec_verify_noalloc_scratch(void** scratch, size_t* bytes);
+
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);
 

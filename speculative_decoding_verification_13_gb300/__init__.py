@@ -26,7 +26,8 @@ import threading
 import torch
 
 __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
-           "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K"]
+           "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
+           "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -36,6 +37,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_MAX_K = 32
 SV_TOPK_MAX = 256
 SV_VOCAB_MAX = 1 << 22
+SV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 ERROR_NAMES = {
     0: "SV_OK", 1: "SV_ERR_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
@@ -261,3 +263,58 @@ def dump_rows(workspace, batch, target_rows, draft_rows, stream=None):
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_dump_rows")
     return dict(stats=stats, kept_count=kept, kept_idx=kidx, kept_p=kp)
+
+
+def _noalloc_lib():
+    lib = load_library()
+    f = lib.spec_verify_noalloc
+    if f.argtypes is None:
+        P = ctypes.c_void_p
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.POINTER(_Logits), ctypes.POINTER(_Logits), P, P, P, P, P, P, P, P,
+                      P, ctypes.c_int32, ctypes.POINTER(_Options)]
+        g = lib.spec_verify_noalloc_scratch
+        g.restype = ctypes.c_int
+        g.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_size_t)]
+    return lib
+
+
+def noalloc_scratch():
+    """``(device address, bytes)`` of the current device's library-owned buffer
+    used by :func:`verify_noalloc`."""
+    ptr, nbytes = ctypes.c_void_p(), ctypes.c_size_t()
+    rc = _noalloc_lib().spec_verify_noalloc_scratch(ctypes.byref(ptr), ctypes.byref(nbytes))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_noalloc_scratch")
+    return ptr.value, nbytes.value
+
+
+def verify_noalloc(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k=None,
+                   top_p=None, *, out_accept_len, out_tokens, out_pq=None, stream=None):
+    """spec_verify_noalloc: verification with the library's own fixed buffer as
+    workspace.  The outputs are caller-provided (nothing is allocated here);
+    calls that can overlap on one device race on the shared buffer."""
+    lib = _noalloc_lib()
+    B = int(k_per_req.shape[0])
+    for t, name, dt in ((k_per_req, "k_per_req", torch.int32),
+                        (temperature, "temperature", torch.float32),
+                        (uniforms, "uniforms", torch.float32),
+                        (draft_tokens, "draft_tokens", torch.int32),
+                        (top_k, "top_k", torch.int32), (top_p, "top_p", torch.float32),
+                        (out_accept_len, "out_accept_len", torch.int32),
+                        (out_tokens, "out_tokens", torch.int32)):
+        _check(t, name, dt)
+    td = _logits_desc(target)
+    dd = _logits_desc(draft, td.vocab)
+    if draft is None:
+        dd.rows = td.rows - B
+        dd.dtype = td.dtype
+    opts = _Options(_ptr(out_pq), None, None) if out_pq is not None else None
+    rc = lib.spec_verify_noalloc(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
+                                 _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                                 _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
+                                 _stream_handle(stream), B,
+                                 ctypes.byref(opts) if opts is not None else None)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_noalloc")
+    return out_accept_len, out_tokens
