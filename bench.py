@@ -1,6 +1,6 @@
 """Benchmark: batched speculative-decoding verification on GB300.
 
-One step = one spec_verify call (setup, row pass, finalize) over the
+One step = one spec_verify call (setup, row pass, filter/decide, draw) over the
 B=256, k=15, V=151936 bfloat16 batch with top-k 50 / top-p 0.9 on both
 distributions (2.41 GB of logits, far larger than the 129 MB L2, so no flush is
 needed between steps).  Prints ONE JSON line.
@@ -367,7 +367,7 @@ def main():
                      "traffic": traffic, "peak_source": peak_src,
                      "bytes_per_launch": bytes_per_step, "launch_ms": rowpass_ms},
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 4 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }

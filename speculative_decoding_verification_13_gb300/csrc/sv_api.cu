@@ -1,5 +1,6 @@
 // Host side of the C ABI: argument validation, workspace layout, and the
-// three launches (setup -> row pass -> finalize) on the caller's stream.
+// four launches (setup -> row pass -> filter / decide -> draw pass) on the
+// caller's stream.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -11,7 +12,9 @@
 
 namespace sv {
 cudaError_t rowpass_configure();
-cudaError_t finalize_configure();
+cudaError_t filter_occupancy(int* occ);
+cudaError_t draw_configure();
+cudaError_t draw_occupancy(int V, int* occ);
 }  // namespace sv
 
 using namespace sv;
@@ -22,14 +25,18 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
   int sms = 0;
+  int occ_filter = 1;  // resident filter / decide CTAs per SM
+  int occ_draw = 1;    // resident draw CTAs per SM for vocabulary draw_v
+  int draw_v = -1;
   bool ready = false;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// Per-device one-time set-up: SM count and the kernels' shared-memory limits.
-int prepare_device(int* sms) {
+// Per-device set-up: SM count, the kernels' shared-memory limits and the
+// post-pass kernels' occupancy (the draw pass's depends on the vocabulary).
+int prepare_device(int vocab, DeviceState* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -37,12 +44,21 @@ int prepare_device(int* sms) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       return SV_ERR_CUDA;
-    if (rowpass_configure() != cudaSuccess || finalize_configure() != cudaSuccess)
+    int of = 1;
+    if (rowpass_configure() != cudaSuccess || draw_configure() != cudaSuccess ||
+        filter_occupancy(&of) != cudaSuccess)
       return SV_ERR_CUDA;
     g_dev[dev].sms = n;
+    g_dev[dev].occ_filter = of;
     g_dev[dev].ready = true;
   }
-  *sms = g_dev[dev].sms;
+  if (g_dev[dev].draw_v != vocab) {
+    int od = 1;
+    if (draw_occupancy(vocab, &od) != cudaSuccess) return SV_ERR_CUDA;
+    g_dev[dev].occ_draw = od;
+    g_dev[dev].draw_v = vocab;
+  }
+  *out = g_dev[dev];
   return SV_OK;
 }
 
@@ -90,8 +106,9 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
     return SV_ERR_WORKSPACE;
   if (batch == 0) return SV_OK;
 
-  int sms = 0;
-  if (int rc = prepare_device(&sms)) return rc;
+  DeviceState ds;
+  if (int rc = prepare_device(t.vocab, &ds)) return rc;
+  const int sms = ds.sms;
 
   Problem P;
   P.target = t.data;
@@ -126,7 +143,15 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   if (options && options->event_rowpass_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
     return SV_ERR_CUDA;
-  if (launch_finalize(P, t.dtype == SV_BF16, s) != cudaSuccess) return SV_ERR_CUDA;
+  const bool bf16 = t.dtype == SV_BF16;
+  const int64_t fjobs = rows;  // at most one job per row
+  const int64_t fmax = int64_t(sms) * ds.occ_filter;
+  if (launch_filter_decide(P, bf16, int(fjobs < fmax ? fjobs : fmax), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const int64_t djobs = batch;  // at most one queued draw per request
+  const int64_t dmax = int64_t(sms) * ds.occ_draw;
+  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 

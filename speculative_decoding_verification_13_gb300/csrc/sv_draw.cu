@@ -1,0 +1,425 @@
+// Draw pass: the final token of every unfiltered sampled request, by inverse
+// CDF in vocabulary-index order, y* = min{ y : C_y > u_k S }, over
+//   the normalised residual max(0, p_L - q_L) after a rejection at L
+//     ("FlashMap…" §4 step 3; "DFlash" §4), or
+//   p_k after a full acceptance (the bonus token).
+//
+// Persistent CTAs, one queued request at a time per CTA.  As in the row pass,
+// warp 0 is a producer that streams the request's target row (and draft row,
+// for a residual) through a 4-stage shared-memory ring with TMA bulk copies
+// (cp.async.bulk, one 8 KB piece of each row per stage, completing on a
+// "full" mbarrier; consumer warps release stages on an "empty" mbarrier).
+// The 8 consumer warps turn each 256-element tile into its weight sum (float,
+// a warp scan); once the row is done, one warp adds the tile sums in tile
+// order (double), finds the tile where the prefix first exceeds t = u_k S and
+// scans that tile's elements (re-read from global memory, L2-resident).  The
+// producer runs ahead into the next request while the consumers locate.
+// Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops,
+// and lets the copies it issued land before exiting.
+#include <math.h>
+
+#include "sv_internal.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kDStages = 4;
+constexpr int kDHalf = 8192;                  // bytes of one row per stage
+constexpr int kDStageBytes = 2 * kDHalf;      // target piece, then draft piece
+constexpr int kDConsumerWarps = 8;
+constexpr int kDConsumers = kDConsumerWarps * 32;
+constexpr int kDThreads = kDConsumers + 32;
+constexpr int kDTile = 256;                   // elements per tile (32 lanes x 8)
+constexpr uint32_t kFull = 0xffffffffu;
+
+// Weight of element y.
+//   kind 0: bonus, exp((x_t - m_t)/T)             (unnormalised p_k)
+//   kind 1: residual, max(0, p_t - q_t)
+//   kind 2: residual fallback, p_t
+struct Weights {
+  float mt, ist, md, isd, c2;
+  int kind;
+  __device__ __forceinline__ float operator()(float xt, float xd) const {
+    const float et = ex2_approx((xt - mt) * c2);
+    if (kind == 0) return et;
+    if (kind == 2) return et * ist;
+    const float ed = ex2_approx((xd - md) * c2);
+    return fmaxf(0.f, et * ist - ed * isd);
+  }
+};
+
+template <bool BF16>
+struct Elt;
+
+template <>
+struct Elt<true> {
+  static constexpr int kSize = 2;
+  // 8 elements from 16 aligned bytes
+  __device__ static void vec8(const void* p, float* x) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    x[0] = bf16_lo(q.x); x[1] = bf16_hi(q.x); x[2] = bf16_lo(q.y); x[3] = bf16_hi(q.y);
+    x[4] = bf16_lo(q.z); x[5] = bf16_hi(q.z); x[6] = bf16_lo(q.w); x[7] = bf16_hi(q.w);
+  }
+  __device__ static float one(const void* p, int64_t i) {
+    return __uint_as_float(uint32_t(static_cast<const uint16_t*>(p)[i]) << 16);
+  }
+};
+
+template <>
+struct Elt<false> {
+  static constexpr int kSize = 4;
+  __device__ static void vec8(const void* p, float* x) {
+    const float4 a = reinterpret_cast<const float4*>(p)[0];
+    const float4 b = reinterpret_cast<const float4*>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+  __device__ static float one(const void* p, int64_t i) {
+    return static_cast<const float*>(p)[i];
+  }
+};
+
+// 8 elements starting at e (a multiple of 8): from `fast` (16-byte aligned
+// memory holding element e at its start) when all 8 lie below `fast_end`,
+// else one by one: below fast_end from `fast`, below V from the row in
+// global memory, -inf past V.
+template <bool BF16>
+__device__ __forceinline__ void elems8(const unsigned char* fast, const void* row, int e,
+                                       int fast_end, int V, float* x) {
+  if (e + 8 <= fast_end) {
+    Elt<BF16>::vec8(fast, x);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = e + q;
+      x[q] = i < fast_end ? Elt<BF16>::one(fast, q)
+                          : (i < V ? Elt<BF16>::one(row, i) : -INFINITY);
+    }
+  }
+}
+
+struct DrawPassShared {
+  double S;
+  double R;
+  int tstar;
+  int fallback;
+  int cabort;
+  int pabort;
+};
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const int* f1,
+                                         const int* f2, uint32_t sleep_ns) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u &&
+        (*reinterpret_cast<const volatile int*>(f1) || *reinterpret_cast<const volatile int*>(f2)))
+      return false;
+    __nanosleep(sleep_ns);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void draw_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kDConsumers) : "memory");
+}
+
+__device__ __forceinline__ double warp_scan_d(double v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_scan_f(float v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
+  using E = Elt<BF16>;
+  constexpr int kEPS = kDHalf / E::kSize;  // elements of a row per stage
+  constexpr int kTPS = kEPS / kDTile;      // tiles per stage
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ DrawPassShared S;
+  unsigned char* ring = smem;
+  const uint32_t full0 = smem_addr(smem + size_t(kDStages) * kDStageBytes);
+  const uint32_t empty0 = full0 + 8u * kDStages;
+  float* ts = reinterpret_cast<float*>(smem + size_t(kDStages) * kDStageBytes + 16 * kDStages);
+  const Ws& w = P.ws;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(full0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, kDConsumerWarps);
+    }
+    fence_mbar_init();
+    S.cabort = 0;
+    S.pabort = 0;
+  }
+  __syncthreads();
+  const int n_draw = w.hdr->n_draw;
+  const int V = P.V;
+  const int ntile = (V + kDTile - 1) / kDTile;
+  const int64_t bulk = (int64_t(V) * E::kSize) & ~int64_t(15);
+  const int nst = int((bulk + kDHalf - 1) / kDHalf);
+  const int fast_end = int(bulk / E::kSize);  // elements the bulk copies deliver
+
+  // ------------------------------------------------------------- producer
+  if (warp == 0) {
+    if (lane != 0) return;
+    uint32_t stage = 0, phase = 0;
+    long long issued = 0;
+    bool stop = false;
+    for (int q = blockIdx.x; q < n_draw && !stop; q += gridDim.x) {
+      const DrawDesc d = w.draw[q];
+      const char* tsrc = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
+      const char* dsrc = d.kind == 1 ? static_cast<const char*>(P.draft) +
+                                           (d.dr - P.Rt) * P.d_stride * E::kSize
+                                     : nullptr;
+      for (int s = 0; s < nst; ++s) {
+        const int64_t rem = bulk - int64_t(s) * kDHalf;
+        const uint32_t bytes = uint32_t(rem < kDHalf ? rem : kDHalf);
+        if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
+          *reinterpret_cast<volatile int*>(&S.pabort) = 1;
+          record_error(w.hdr, SV_ERR_TIMEOUT, -1, d.tr);
+          stop = true;
+          break;
+        }
+        const uint32_t full = full0 + 8u * stage;
+        mbar_arrive_expect_tx(full, dsrc ? 2u * bytes : bytes);
+        unsigned char* dst = ring + size_t(stage) * kDStageBytes;
+        bulk_load(smem_addr(dst), tsrc + int64_t(s) * kDHalf, bytes, full);
+        if (dsrc) bulk_load(smem_addr(dst + kDHalf), dsrc + int64_t(s) * kDHalf, bytes, full);
+        ++issued;
+        if (++stage == kDStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (stop || *reinterpret_cast<volatile int*>(&S.cabort)) {
+      // Let every copy this CTA issued land before the CTA may exit.
+      const long long first = issued > kDStages ? issued - kDStages : 0;
+      for (long long g = first; g < issued; ++g) {
+        const uint32_t st = uint32_t(g % kDStages), ph = uint32_t((g / kDStages) & 1);
+        for (uint32_t it = 0; it < kWaitLimit; ++it)
+          if (mbar_try_wait(full0 + 8u * st, ph)) break;
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------- consumers
+  const int cwarp = warp - 1;
+  uint32_t stage = 0, phase = 0;
+  for (int q = blockIdx.x; q < n_draw; q += gridDim.x) {
+    const DrawDesc d = w.draw[q];
+    Weights W;
+    W.mt = d.mt;
+    W.ist = d.ist;
+    W.md = d.md;
+    W.isd = d.isd;
+    W.c2 = d.c2;
+    W.kind = d.kind;
+    const void* trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
+    const void* drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
+                                         (d.dr - P.Rt) * P.d_stride * E::kSize
+                                   : nullptr;
+    // tile sums: the tiles of each stage as it lands
+    for (int s = 0; s < nst; ++s) {
+      if (!wait_bar(full0 + 8u * stage, phase, &S.cabort, &S.pabort, 16)) {
+        *reinterpret_cast<volatile int*>(&S.cabort) = 1;
+        record_error(w.hdr, SV_ERR_TIMEOUT, -1, d.tr);
+      }
+      if (!*reinterpret_cast<volatile int*>(&S.cabort)) {
+        const unsigned char* tp = ring + size_t(stage) * kDStageBytes;
+        for (int i = cwarp; i < kTPS; i += kDConsumerWarps) {
+          const int tau = s * kTPS + i;
+          if (tau >= ntile) break;
+          const int e = tau * kDTile + lane * 8;
+          const int off = (i * kDTile + lane * 8) * E::kSize;
+          float xt[8], xd[8];
+          elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
+          if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
+          float ls = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+          const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
+          if (lane == 0) ts[tau] = tsum;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+      if (++stage == kDStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // tiles past the bulk-copied part of the row, from global memory
+    for (int tau = nst * kTPS + cwarp; tau < ntile; tau += kDConsumerWarps) {
+      const int e = tau * kDTile + lane * 8;
+      float xt[8], xd[8];
+      elems8<BF16>(nullptr, trow, e, 0, V, xt);
+      if (W.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
+      float ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+      const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
+      if (lane == 0) ts[tau] = tsum;
+    }
+    draw_sync();
+    if (*reinterpret_cast<volatile int*>(&S.cabort)) break;
+    // total S, in tile order
+    if (cwarp == 0) {
+      double tot = 0.0;
+      for (int t0 = 0; t0 < ntile; t0 += 32) {
+        const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
+        tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
+      }
+      if (lane == 0) {
+        S.S = tot;
+        S.fallback = W.kind == 1 && !(tot > 0.0);
+      }
+    }
+    draw_sync();
+    if (S.fallback) {
+      // residual mass vanished through rounding: draw from p_L
+      W.kind = 2;
+      for (int tau = cwarp; tau < ntile; tau += kDConsumerWarps) {
+        const int e = tau * kDTile + lane * 8;
+        float xt[8];
+        elems8<BF16>(nullptr, trow, e, 0, V, xt);
+        float ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls += W(xt[k], 0.f);
+        const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
+        if (lane == 0) ts[tau] = tsum;
+      }
+      draw_sync();
+      if (cwarp == 0) {
+        double tot = 0.0;
+        for (int t0 = 0; t0 < ntile; t0 += 32) {
+          const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
+          tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
+        }
+        if (lane == 0) S.S = tot;
+      }
+      draw_sync();
+    }
+    if (cwarp == 0) {
+      // the tile where the prefix first exceeds t, then the element in it
+      const double t = d.u * S.S;
+      double carry = 0.0, R = 0.0, Rlast = 0.0;
+      int tstar = -1, tlast = -1;
+      for (int t0 = 0; t0 < ntile && tstar < 0; t0 += 32) {
+        const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
+        const double incl = warp_scan_d(v) + carry;
+        double ex = __shfl_up_sync(kFull, incl, 1);
+        if (lane == 0) ex = carry;
+        const uint32_t pos = __ballot_sync(kFull, v > 0.0);
+        const uint32_t hit = __ballot_sync(kFull, t0 + lane < ntile && incl > t);
+        if (pos) {
+          const int l = 31 - __clz(pos);
+          tlast = t0 + l;
+          Rlast = __shfl_sync(kFull, ex, l);
+        }
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          tstar = t0 + l;
+          R = __shfl_sync(kFull, ex, l);
+        }
+        carry = __shfl_sync(kFull, incl, 31);
+      }
+      if (tstar < 0) {  // t beyond every prefix (rounding): the last tile with mass
+        tstar = tlast;
+        R = Rlast;
+      }
+      int y = -1;
+      if (tstar >= 0) {
+        const int base = tstar * kDTile + lane * 8;
+        float xt[8], xd[8], r[8];
+        elems8<BF16>(nullptr, trow, base, 0, V, xt);
+        if (W.kind == 1) elems8<BF16>(nullptr, drow, base, 0, V, xd);
+        float ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          r[k] = W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+          ls += r[k];
+        }
+        const float inc = warp_scan_f(ls);
+        float exf = __shfl_up_sync(kFull, inc, 1);
+        if (lane == 0) exf = 0.f;
+        int ye = INT_MAX, lastp = -1;
+        float pre = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          pre += r[k];
+          if (r[k] > 0.f) lastp = base + k;
+          if (ye == INT_MAX && r[k] > 0.f && R + double(exf + pre) > t) ye = base + k;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ye = min(ye, __shfl_xor_sync(kFull, ye, o));
+          lastp = max(lastp, __shfl_xor_sync(kFull, lastp, o));
+        }
+        y = ye != INT_MAX ? ye : lastp;
+      }
+      if (lane == 0) {
+        if (y < 0) record_error(w.hdr, SV_ERR_INTERNAL, -1, d.tr);  // no mass found
+        P.out_tokens[d.t0 + d.L] = y;
+      }
+    }
+    draw_sync();  // tile sums are rewritten by the next request
+  }
+}
+
+}  // namespace
+
+size_t draw_pass_smem_bytes(int V) {
+  return size_t(kDStages) * kDStageBytes + 16 * kDStages +
+         sizeof(float) * size_t((V + kDTile - 1) / kDTile);
+}
+
+cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s) {
+  const size_t smem = draw_pass_smem_bytes(P.V);
+  if (bf16)
+    draw_pass_kernel<true><<<grid, kDThreads, smem, s>>>(P);
+  else
+    draw_pass_kernel<false><<<grid, kDThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+// Shared-memory limit (largest vocabulary) and resident CTAs per SM for a
+// vocabulary of V (host queries; nothing is allocated).
+cudaError_t draw_configure() {
+  const int smem = int(draw_pass_smem_bytes(SV_VOCAB_MAX));
+  cudaError_t e = cudaFuncSetAttribute(draw_pass_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(draw_pass_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+cudaError_t draw_occupancy(int V, int* occ) {
+  int a = 0, b = 0;
+  const size_t smem = draw_pass_smem_bytes(V);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, draw_pass_kernel<true>,
+                                                                kDThreads, smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, draw_pass_kernel<false>, kDThreads,
+                                                      smem);
+  if (e != cudaSuccess) return e;
+  *occ = max(1, min(a, b));
+  return cudaSuccess;
+}
+
+}  // namespace sv

@@ -23,9 +23,6 @@ constexpr int kRegion = kBufCap / kConsumerWarps;        // per-warp region (fas
 constexpr int kRawCap = 1024;                            // top-k survivors kept per row
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
-constexpr int kFinalThreads = 512;
-constexpr int kFinalTileElems = kFinalThreads * 8;       // elements per scan tile
-constexpr int kMaxFinalTiles = (SV_VOCAB_MAX + kFinalTileElems - 1) / kFinalTileElems;
 constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
 
 // Row modes chosen per request by the setup kernel.
@@ -38,7 +35,9 @@ struct WsHeader {
   int64_t err_row;
   int32_t n_active;     // rows the row pass must stream
   int32_t global_err;   // batch-level data error (row counts)
-  int32_t pad[10];
+  int32_t n_jobs;       // filter / decide jobs listed by the setup kernel
+  int32_t n_draw;       // requests queued for the unfiltered draw
+  int32_t pad[8];
 };
 
 struct RowStat {
@@ -50,6 +49,17 @@ struct RowStat {
   int32_t mode;
 };
 
+// What the unfiltered draw of one request needs (written by its decide job).
+struct DrawDesc {
+  int64_t tr, dr;  // target row p_L, draft row q_L (residual only)
+  float mt, ist;   // target row max and 1 / normaliser
+  float md, isd;   // draft row max and 1 / normaliser
+  float c2;        // log2(e) / T
+  int32_t kind;    // 0 bonus p_k, 1 residual max(0, p_L - q_L), 2 residual fallback p_L
+  double u;        // the final uniform u_k
+  int32_t t0, L;
+};
+
 struct Ws {
   WsHeader* hdr;
   int32_t* t_off;    // [B + 1]
@@ -59,10 +69,15 @@ struct Ws {
   int32_t* cand_idx; // [R, kTopkMax]
   double* cand_p;    // [R, kTopkMax]
   uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys)
+  int4* job;          // [R] {request, row i of the request (0..2k) or -1 for a
+                      //      decide job, logit row, the row's draft token or -1}
+  int32_t* req_cnt;   // [B] filtered rows finished
+  DrawDesc* draw;     // [B] queued draws, in queue order
 };
 
 struct WsLayout {
-  size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, off_raw, total;
+  size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, off_raw, off_job,
+      off_rcnt, off_draw, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -78,6 +93,10 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   L.off_cidx = o;    o = align256(o + sizeof(int32_t) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_cp = o;      o = align256(o + sizeof(double) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_raw = o;     o = align256(o + sizeof(uint64_t) * kRawCap * (size_t)(R > 0 ? R : 1));
+  const size_t B1 = (size_t)(B > 0 ? B : 1);
+  L.off_job = o;     o = align256(o + sizeof(int4) * (size_t)(R > 0 ? R : 1));
+  L.off_rcnt = o;    o = align256(o + sizeof(int32_t) * B1);
+  L.off_draw = o;    o = align256(o + sizeof(DrawDesc) * B1);
   L.total = o;
   return L;
 }
@@ -93,6 +112,9 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.cand_idx = reinterpret_cast<int32_t*>(p + L.off_cidx);
   w.cand_p = reinterpret_cast<double*>(p + L.off_cp);
   w.cand_raw = reinterpret_cast<uint64_t*>(p + L.off_raw);
+  w.job = reinterpret_cast<int4*>(p + L.off_job);
+  w.req_cnt = reinterpret_cast<int32_t*>(p + L.off_rcnt);
+  w.draw = reinterpret_cast<DrawDesc*>(p + L.off_draw);
   return w;
 }
 
@@ -119,7 +141,8 @@ struct Problem {
 // ------------------------------------------------------- host-side launchers
 cudaError_t launch_setup(const Problem& P, cudaStream_t s);
 cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s);
-cudaError_t launch_finalize(const Problem& P, bool bf16, cudaStream_t s);
+cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 size_t rowpass_smem_bytes();
 
 // ------------------------------------------------------------ device helpers

@@ -1,7 +1,8 @@
 // Setup kernel: one CTA per call.  Computes the ragged row offsets
 // t_off[b] = sum_{j<b} (k_j + 1), validates every request's parameters and
-// drafted tokens, picks each row's mode and writes the list of rows the
-// streaming pass must read, ordered by request.
+// drafted tokens, picks each row's mode, writes the list of rows the
+// streaming pass must read (ordered by request) and the list of post-pass jobs,
+// and zeroes the per-request counters the post-pass kernels count with.
 #include "sv_internal.cuh"
 
 namespace sv {
@@ -46,6 +47,8 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     w.hdr->err_row = -1;
     w.hdr->n_active = 0;
     w.hdr->global_err = 0;
+    w.hdr->n_jobs = 0;
+    w.hdr->n_draw = 0;
     s_bad = 0;
   }
   __syncthreads();
@@ -81,8 +84,10 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   __syncthreads();
   if (s_bad) return;
 
-  // Pass 2: per-request validation, modes, and the active row list.
-  int carry_a = 0;
+  // Pass 2: per-request validation, modes, the active row list and the
+  // post-pass job list (2k + 1 filter jobs for a filtered request, one decide
+  // job for any other).
+  int carry_a = 0, carry_j = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int code = 0, active = 0, mode_t = kSkip, mode_d = kSkip, k = 0, t0 = 0, d0 = 0;
@@ -119,9 +124,24 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
         active = 2 * k + 1;
       }
     }
-    int tot;
+    const bool filt = !code && mode_t == kTopk;
+    const int njob = b < P.B ? (filt ? 2 * k + 1 : 1) : 0;
+    int tot, totj;
     const int a0 = carry_a + block_exclusive_scan(active, &tot);
     carry_a += tot;
+    const int j0 = carry_j + block_exclusive_scan(njob, &totj);
+    carry_j += totj;
+    if (b < P.B) {
+      if (filt) {
+        for (int i = 0; i <= k; ++i)
+          w.job[j0 + i] = make_int4(b, i, t0 + i, i < k ? P.draft_tokens[d0 + i] : -1);
+        for (int i = 0; i < k; ++i)
+          w.job[j0 + k + 1 + i] = make_int4(b, k + 1 + i, int(P.Rt) + d0 + i, P.draft_tokens[d0 + i]);
+      } else {
+        w.job[j0] = make_int4(b, -1, 0, -1);
+      }
+      w.req_cnt[b] = 0;
+    }
     if (b < P.B && active) {
       int a = a0;
       for (int i = 0; i <= k; ++i) {
@@ -146,7 +166,10 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       }
     }
   }
-  if (threadIdx.x == 0) w.hdr->n_active = carry_a;
+  if (threadIdx.x == 0) {
+    w.hdr->n_active = carry_a;
+    w.hdr->n_jobs = carry_j;
+  }
 }
 
 }  // namespace

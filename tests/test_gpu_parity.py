@@ -109,7 +109,9 @@ def test_filtered_kept_sets_match_oracle():
         n = int(d["kept_count"][r])
         idx = d["kept_idx"][r, :n].numpy()
         assert sorted(idx.tolist()) == nz.tolist(), r
-        np.testing.assert_allclose(d["kept_p"][r, :n].numpy(), p[idx], rtol=1e-12, atol=0)
+        # float-accurate weights (a few 1e-7 relative), well inside the 1e-5
+        # relative bound on softmax probabilities
+        np.testing.assert_allclose(d["kept_p"][r, :n].numpy(), p[idx], rtol=1e-6, atol=0)
         # kept order is (logit desc, index asc)
         vals = rows[r].float().numpy()[idx]
         assert all((vals[i] > vals[i + 1]) or (vals[i] == vals[i + 1] and idx[i] < idx[i + 1])
