@@ -65,6 +65,17 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x, pg, device):
+    """Max of a per-rank float over the process group: the step time of a
+    weak-scaling run is the slowest rank's (nccl on the GPU, gloo in tests)."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
 def kernel_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -256,11 +267,7 @@ def measure_e2e(args, batch, v, acc, tok, stream, dev, pg):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, pg, dev)
     del dbuf, host
     return {"value": ws * Rt / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms}
@@ -327,10 +334,7 @@ def main():
     rowpass_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     clk = clocks.stop() if clocks else None
 
-    if pg:
-        t = torch.tensor([step_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, pg, dev)
 
     e2e = None if args.no_e2e else measure_e2e(args, batch, v, acc, tok, stream, dev, pg)
     if rank != 0:
