@@ -1,27 +1,26 @@
 // Row pass: the one kernel that streams every logit row from HBM once.
 //
-// Persistent, one CTA per SM.  Warp 0 is the producer: it walks the CTA's
-// share of the active-row list and issues TMA bulk copies (cp.async.bulk,
-// 16 KB each) into an 8-stage shared-memory ring, each stage guarded by a
-// "full" mbarrier (transaction bytes) and an "empty" mbarrier (one arrival per
-// consumer warp).  Warps 1..16 consume the tiles and reduce each row in one of
-// three modes (chosen per request by the setup kernel):
+// Persistent, two CTAs per SM.  Warp 0 is the producer: one lane walks the
+// CTA's share of the active-row list and issues TMA bulk copies
+// (cp.async.bulk, 16 KB each) into a 4-stage shared-memory ring, each stage
+// guarded by a "full" mbarrier (transaction bytes) and an "empty" mbarrier (one
+// arrival per consumer warp).  Warps 1..8 consume the tiles and reduce each row
+// in one of three modes (chosen per request by the setup kernel):
 //   kStats  - temperature softmax statistics of a sampled, unfiltered row: the
 //             row max M and S = sum_y exp((x_y - M) / T) by an online
 //             (running-max, rescaled) sum; then p(x) = exp((x_x - M) / T) / S
 //             of the row's draft token in double precision.
 //             ("FlashMap…" §5 draft_block step 5: logits / T, softmax.)
 //   kArgmax - greedy: argmax of the raw logits, lowest index on ties.
-//   kTopk   - the top-k tokens in (logit desc, index asc) order, selected with
-//             a running threshold: a tile's candidates are counted, and
-//             inserted into a shared buffer only if they beat the threshold;
-//             the threshold is seeded from the k-th largest per-vector maximum
-//             of the first tile and tightened by exact radix selection when
-//             the buffer fills.  The epilogue applies the temperature softmax
-//             over the survivors, the top-p cut and the renormalisation in
-//             double precision ("Speculative decoding and multi-token
-//             prediction", "Why the output is identical": the same filter on
-//             both distributions).
+//   kTopk   - the top-k candidates of a filtered row: a speculative threshold
+//             from the first tile (the r-th largest per-vector maximum), then
+//             every tile's vectors are flagged against it and the candidates
+//             are appended to per-warp shared queues; the survivors (at least
+//             k, at most kRawCap) are published unsorted for the filter
+//             kernel, which selects the exact top k.  A failed speculation is
+//             redone exactly from global memory (certified radix selection).
+//             ("Speculative decoding and multi-token prediction", "Why the
+//             output is identical": the same filter on both distributions.)
 // Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops
 // issuing copies, lets the copies it issued land, and exits.
 #include <math.h>
