@@ -81,8 +81,12 @@ struct Elt<true> {
   }
   // Largest element; NaN if any element is NaN.
   __device__ static float vmax(const uint4& q) {
-    const uint32_t m = bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
+    const uint32_t m = pmax(q);
     return fmax_nan(bf16_lo(m), bf16_hi(m));
+  }
+  // Packed maxima (even elements, odd elements) as bf16x2; NaN propagates.
+  __device__ static uint32_t pmax(const uint4& q) {
+    return bmax2_nan(bmax2_nan(q.x, q.y), bmax2_nan(q.z, q.w));
   }
   __device__ static float scalar(const void* row, int64_t i) {
     return __uint_as_float(uint32_t(static_cast<const uint16_t*>(row)[i]) << 16);
@@ -133,6 +137,37 @@ __device__ __forceinline__ int nth_set_bit(uint32_t x, int n) {
     }
   }
   return pos;
+}
+
+// A bf16 value d below v (v itself a bf16 value), in both halves of a
+// bf16x2, such that every packed element h >= v has max(h, d) != d: the next
+// bf16 below v, or -(smallest normal) when v is zero or subnormal (so that the
+// comparison never hinges on a subnormal, which the packed max may treat as
+// zero).  Elements between d and v are flagged too; flags are only a filter,
+// the exact key comparison decides.  For v = -inf, and for the NaN that the
+// empty threshold (key 0) decodes to, the pattern is a NaN, so every element
+// is flagged.
+__device__ __forceinline__ uint32_t bf16_below2(float v) {
+  if (v != v) return 0xff81ff81u;
+  const uint32_t b = __float_as_uint(v) >> 16;
+  const uint32_t d = (b & 0x7f80u) == 0u ? 0x8080u : ((b & 0x8000u) ? b + 1u : b - 1u);
+  return d | (d << 16);
+}
+
+// Descending bitonic sort of the 32 floats a warp holds, one per lane.
+__device__ __forceinline__ float warp_sort_desc_f32(float u) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, u, j);
+      const bool desc = (lane & size) == 0;
+      const bool lower = (lane & j) == 0;
+      u = (desc == lower) ? fmaxf(u, o) : fminf(u, o);
+    }
+  }
+  return u;
 }
 
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
@@ -576,14 +611,25 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         int qn = 0;  // flagged vectors of this warp in this tile (warp-uniform)
         if (nvec == kTileBytes / 16) {
           // full tile: two vectors per compare, no bounds checks
+          [[maybe_unused]] uint32_t below2 = 0u;
+          if constexpr (BF16) below2 = bf16_below2(thv);
 #pragma unroll
           for (int i = 0; i < VPT; i += 2) {
             const int va = ctid + i * kConsumers, vb = va + kConsumers;
             const uint4 qa = tile[va], qb = tile[vb];
-            const bool any = !(fmax_nan(E::vmax(qa), E::vmax(qb)) < thv);
+            bool any, ca, cb;
+            if constexpr (BF16) {
+              // packed: a vector is flagged when one of its elements is >= thv
+              const uint32_t ma = E::pmax(qa), mb = E::pmax(qb);
+              any = bmax2_nan(bmax2_nan(ma, mb), below2) != below2;
+              ca = any && bmax2_nan(ma, below2) != below2;
+              cb = any && bmax2_nan(mb, below2) != below2;
+            } else {
+              any = !(fmax_nan(E::vmax(qa), E::vmax(qb)) < thv);
+              ca = any && !(E::vmax(qa) < thv);
+              cb = any && !(E::vmax(qb) < thv);
+            }
             if (__any_sync(0xffffffffu, any)) {
-              const bool ca = any && !(E::vmax(qa) < thv);
-              const bool cb = any && !(E::vmax(qb) < thv);
               const uint32_t ba = __ballot_sync(0xffffffffu, ca);
               if (ca) queue[qn + __popc(ba & lt)] = uint16_t(va);
               qn += __popc(ba);
@@ -641,11 +687,50 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         return composite_key(vm, uint32_t(t * kTileElems + v * EPV + first));
       };
       // Tight speculative threshold from tile 0: each warp extracts the top L
-      // of its vector maxima, the CTA sorts the 8L candidates and takes the
-      // r-th largest.  A speculative threshold needs no exact tie order (the
-      // row-end check decides), so a vector maximum is keyed with the index
-      // of the vector's first element.
+      // of its vector maxima and the r-th largest of the 8L candidates is
+      // taken.  A speculative threshold needs no exact tie order (the row-end
+      // check decides), so it is keyed as the smallest key of its value.  With
+      // 8L <= 32 candidates every warp sorts them itself after one barrier;
+      // larger L take the CTA sort.
       auto bootstrap_spec = [&](const uint4* tile, int nvec, int t, int r, int L) {
+        const int nu = kConsumerWarps * L;
+        if (nu <= 32) {
+          float* cand = reinterpret_cast<float*>(scratch);
+          float mx[VPT];
+#pragma unroll
+          for (int i = 0; i < VPT; ++i) {
+            const int v = ctid + i * kConsumers;
+            const float m = v < nvec ? E::vmax(tile[v]) : -INFINITY;
+            mx[i] = m == m ? m : -INFINITY;  // a NaN row is flagged by the sweep
+          }
+          for (int q = 0; q < L; ++q) {
+            float lm = mx[0];
+            int li = 0;
+#pragma unroll
+            for (int j = 1; j < VPT; ++j)
+              if (mx[j] > lm) {
+                lm = mx[j];
+                li = j;
+              }
+            float wm = lm;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+            if (lane == 0) cand[cwarp * L + q] = wm;
+            // lanes holding the maximum drop it (ties may drop several: the
+            // threshold only gets looser)
+            if (lm == wm) {
+#pragma unroll
+              for (int j = 0; j < VPT; ++j)
+                if (j == li) mx[j] = -INFINITY;
+            }
+          }
+          consumer_sync();
+          const float u = warp_sort_desc_f32(lane < nu ? cand[lane] : -INFINITY);
+          const float thr = __shfl_sync(0xffffffffu, u, r - 1);
+          const uint64_t tb = composite_key(thr, 0xffffffffu);
+          if (tb > theta) theta = tb;
+          return;
+        }
         uint64_t mx[VPT];
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -676,7 +761,6 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           }
         }
         consumer_sync();
-        const int nu = kConsumerWarps * L;
         uint64_t u = ctid < nu ? scratch[ctid] : 0ull;
         u = block_sort_desc<kConsumers>(u, ctid, next_pow2(nu), xchg, ConsumerSync());
         if (ctid == r - 1) S.thmin[2] = u;
