@@ -100,8 +100,10 @@ typedef struct {
 
 /* Optional extras of spec_verify; pass NULL for none. */
 typedef struct {
-  /* [draft_rows, 2] device doubles: (p_i(x_i), q_i(x_i)) of every sampled
-   * request, NaN for greedy and failed requests (parity / diagnostics). */
+  /* [draft_rows, 2] device doubles: (p_i(x_i), q_i(x_i)) of sampled requests
+   * at every position the decision examined (0 .. min(L, k-1)); positions
+   * after the first rejection may be NaN (filtered requests never evaluate
+   * them).  NaN for greedy and failed requests (parity / diagnostics). */
   double* out_pq;
   /* cudaEvent_t handles recorded on the stream right before and right after
    * the row-streaming kernel (profiling); NULL to skip. */
@@ -153,7 +155,9 @@ int spec_verify_get_error(const void* workspace, void* stream, int32_t* code,
  *              row was not filtered)
  *   kept_idx   [R, SV_TOPK_MAX] int32 and kept_p [R, SV_TOPK_MAX] doubles:
  *              the kept tokens in (logit desc, index asc) order and their
- *              renormalised probabilities.
+ *              renormalised probabilities.  Filtered requests evaluate only
+ *              the rows up to their first rejection (and the bonus row after
+ *              k acceptances); other rows' entries are unspecified.
  * Any output pointer may be NULL. */
 int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t batch,
                           int64_t target_rows, int64_t draft_rows, void* stream,

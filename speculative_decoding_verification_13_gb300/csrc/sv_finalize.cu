@@ -33,8 +33,6 @@ namespace {
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr double kFix = 36028797018963968.0;    // 2^55: unit of the kept-set fixed-point sums
                                                 // (<= 256 weights <= 1 stay below 2^63)
-constexpr double kToppGuard = 1e-5;             // relative top-p margin below which the
-                                                // cut is redone in double precision
 
 __device__ __forceinline__ double nan64() { return __longlong_as_double(0x7ff8000000000000LL); }
 
@@ -234,8 +232,12 @@ struct WarpSel {
     unsigned long long before[kTopkMax];  // fixed-point mass before j
   };
   union {
-    double w[kTopkMax];       // weights in sorted order
     uint64_t grp[kTopkMax];   // during selection: the keys of the boundary bin
+    struct {                  // weights in sorted order, wf[j] * 2^we[j]
+      float wf[kTopkMax];
+      int we[kTopkMax];
+    };
+    double wd[kTopkMax];      // weights in double (close top-p calls)
   };
   int digit, above, cnt;
   int pad;
@@ -247,23 +249,59 @@ union WarpScratch {
   DrawScratch draw;
 };
 
-// The K-th largest of n > K unique keys that the lanes hold in registers
-// (lane holds keys r * 32 + lane; 0 marks an empty slot), exactly.  One pass
-// bins the keys into 256 ordered bins, linear in the logit over [min, max]
-// (a monotone map); the bin holding the K-th largest is then resolved among
-// its own keys.  Warp-uniform result.
-__device__ uint64_t select_kth_regs(const uint64_t (&key)[kRegKeys], int K, WarpSel& ws,
-                                    const uint64_t* raw, int n, uint32_t skip) {
+// A row's survivor keys for the selection passes: held in registers (lane
+// holds keys r * 32 + lane), or read from memory 512 at a time with every
+// lane's loads issued together.  each(f) calls f(key) on every slot, in step
+// across the warp (key 0 marks an empty slot).
+struct RegKeys {
+  const uint64_t (&key)[kRegKeys];
+  int nslot;  // slots past it hold no key (warp-uniform)
+  template <class F>
+  __device__ __forceinline__ void each(F f) const {
+#pragma unroll
+    for (int r = 0; r < kRegKeys; ++r) {
+      if (r >= nslot) break;
+      f(key[r]);
+    }
+  }
+};
+
+struct MemKeys {
+  const uint64_t* raw;
+  int n;
+  template <class F>
+  __device__ __forceinline__ void each(F f) const {
+    const int lane = threadIdx.x & 31;
+    for (int c0 = 0; c0 < n; c0 += 32 * kRegKeys) {
+      uint64_t key[kRegKeys];
+#pragma unroll
+      for (int r = 0; r < kRegKeys; ++r) {
+        const int e = c0 + r * 32 + lane;
+        key[r] = e < n ? __ldcg(raw + e) : 0ull;
+      }
+#pragma unroll
+      for (int r = 0; r < kRegKeys; ++r) f(key[r]);
+    }
+  }
+};
+
+// The K-th largest of n > K unique survivor keys, exactly.  One pass bins the
+// keys into 256 ordered bins, linear in the logit over [min, max] (a monotone
+// map); the bin holding the K-th largest is then resolved among its own keys.
+// Warp-uniform result.
+template <class Src>
+__device__ uint64_t select_kth(const Src& src, int K, WarpSel& ws, const uint64_t* raw, int n,
+                               uint32_t skip) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t lo = ~0u, hi = 0u;
-#pragma unroll
-  for (int r = 0; r < kRegKeys; ++r)
-    if (key[r]) {
-      const uint32_t h = uint32_t(key[r] >> 32);
+  src.each([&](uint64_t k) {
+    if (k) {
+      const uint32_t h = uint32_t(k >> 32);
       lo = min(lo, h);
       hi = max(hi, h);
     }
+  });
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
   // bins linear in the logit value (the order-preserving integer image is
@@ -280,9 +318,9 @@ __device__ uint64_t select_kth_regs(const uint64_t (&key)[kRegKeys], int K, Warp
 #pragma unroll
   for (int j = 0; j < 8; ++j) ws.hist[lane * 8 + j] = 0;
   __syncwarp();
-#pragma unroll
-  for (int r = 0; r < kRegKeys; ++r)
-    if (key[r]) atomicAdd(&ws.hist[bin(key[r])], 1);
+  src.each([&](uint64_t k) {
+    if (k) atomicAdd(&ws.hist[bin(k)], 1);
+  });
   __syncwarp();
   // the bin holding the K-th largest, the count above it and its own count
   int cnt[8], loc = 0;
@@ -312,9 +350,9 @@ __device__ uint64_t select_kth_regs(const uint64_t (&key)[kRegKeys], int K, Warp
   if (gcnt == need) {
     // the whole bin is kept: the threshold is its smallest key
     uint64_t mn = ~0ull;
-#pragma unroll
-    for (int r = 0; r < kRegKeys; ++r)
-      if (key[r] && bin(key[r]) == bstar && key[r] < mn) mn = key[r];
+    src.each([&](uint64_t k) {
+      if (k && bin(k) == bstar && k < mn) mn = k;
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const uint64_t y = shfl_xor_u64(mn, o);
@@ -324,13 +362,12 @@ __device__ uint64_t select_kth_regs(const uint64_t (&key)[kRegKeys], int K, Warp
   }
   if (gcnt > kTopkMax) return warp_select_kth(raw, n, K, ws.hist, &ws.digit, skip);
   int g = 0;
-#pragma unroll
-  for (int r = 0; r < kRegKeys; ++r) {
-    const bool in = key[r] && bin(key[r]) == bstar;
+  src.each([&](uint64_t k) {
+    const bool in = k && bin(k) == bstar;
     const uint32_t bal = __ballot_sync(kFull, in);
-    if (in) ws.grp[g + __popc(bal & lt)] = key[r];
+    if (in) ws.grp[g + __popc(bal & lt)] = k;
     g += __popc(bal);
-  }
+  });
   __syncwarp();
   if (gcnt <= 32) {
     uint64_t v[1] = {lane < gcnt ? ws.grp[lane] : 0ull};
@@ -353,10 +390,10 @@ __device__ uint64_t select_kth_regs(const uint64_t (&key)[kRegKeys], int K, Warp
 // softmax over them, the top-p cut and the renormalisation; writes the kept
 // list, the kept size and p(x) of the row's draft token.  Weights are
 // float-accurate (relative error a few 1e-7) with exact fixed-point prefix
-// sums; a top-p cut within kToppGuard of the threshold is redone in double
+// sums; a top-p cut within 2^-17 of the threshold is redone in double
 // precision, so the kept set is the double-precision one.
 template <bool BF16>
-__device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float tp, int gx,
+__device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float tp, int gx,
                                 WarpSel& ws) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
@@ -367,9 +404,20 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
   uint64_t key[kRegKeys];
 #pragma unroll
   for (int r = 0; r < kRegKeys / 2; ++r) key[r] = __ldcg(raw + r * 32 + lane);
-  const int n = w.stats[row].kept;
+  const int n = min(max(w.stats[row].kept, 0), kRawCap);
   const uint32_t skip = BF16 ? kSkipBf16 : kSkipF32;
   int cnt = 0;
+  auto keep_top = [&](const auto& src, uint64_t th) {
+    src.each([&](uint64_t k) {
+      const bool keep = k && k >= th;
+      const uint32_t bal = __ballot_sync(kFull, keep);
+      if (keep) {
+        const int sl = cnt + __popc(bal & lt);
+        if (sl < kTopkMax) ws.list[sl] = k;
+      }
+      cnt += __popc(bal);
+    });
+  };
   if (n <= 32 * kRegKeys) {
 #pragma unroll
     for (int r = 0; r < kRegKeys; ++r) {
@@ -377,30 +425,11 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
       if (r >= kRegKeys / 2) key[r] = e < n ? __ldcg(raw + e) : 0ull;
       else if (e >= n) key[r] = 0ull;  // keys are never 0
     }
-    const uint64_t th = n > K ? select_kth_regs(key, K, ws, raw, n, skip) : 0ull;
-#pragma unroll
-    for (int r = 0; r < kRegKeys; ++r) {
-      const bool keep = key[r] && key[r] >= th;
-      const uint32_t bal = __ballot_sync(kFull, keep);
-      if (keep) {
-        const int sl = cnt + __popc(bal & lt);
-        if (sl < kTopkMax) ws.list[sl] = key[r];
-      }
-      cnt += __popc(bal);
-    }
+    const RegKeys src{key, (n + 31) >> 5};
+    keep_top(src, n > K ? select_kth(src, K, ws, raw, n, skip) : 0ull);
   } else {
-    const uint64_t th = n > K ? warp_select_kth(raw, n, K, ws.hist, &ws.digit, skip) : 0ull;
-    for (int base = 0; base < n; base += 32) {
-      const int e = base + lane;
-      const uint64_t key = e < n ? __ldcg(raw + e) : 0ull;
-      const bool keep = e < n && key >= th;
-      const uint32_t bal = __ballot_sync(kFull, keep);
-      if (keep) {
-        const int sl = cnt + __popc(bal & lt);
-        if (sl < kTopkMax) ws.list[sl] = key;
-      }
-      cnt += __popc(bal);
-    }
+    const MemKeys src{raw, n};
+    keep_top(src, n > K ? select_kth(src, K, ws, raw, n, skip) : 0ull);
   }
   const int nsel = min(cnt, K);
   const int Psz = max(32, next_pow2(nsel > 0 ? nsel : 1));
@@ -411,55 +440,60 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
   const float v0 = composite_value(ws.list[0]);
   const double cd = 1.4426950408889634 / double(T);
   const float chi = float(cd), clo = float(cd - double(chi));
-  // weights and the fixed-point mass before each j
+  // weights and the fixed-point mass before each j (integer work; the FP64
+  // pipe, scarce on this part, is kept for a few operations per row)
   unsigned long long W = 0ull;
   for (int j0 = 0; j0 < nsel; j0 += 32) {
     const int j = j0 + lane;
     unsigned long long fx = 0ull;
     if (j < nsel) {
       const float v = composite_value(ws.list[j]);
-      double wd = 0.0;
+      float f = 0.f;
+      int e2 = 0;
       if (v > -INFINITY) {
-        int e2;
-        const float f = weight_split(v, v0, chi, clo, &e2);
-        wd = scale2(double(f), e2);
+        f = weight_split(v, v0, chi, clo, &e2);
         fx = fix55(f, e2);
       }
-      ws.w[j] = wd;
+      ws.wf[j] = f;
+      ws.we[j] = e2;
     }
     const unsigned long long incl = warp_incl_scan(fx);
     if (j < nsel) ws.before[j] = W + incl - fx;
     W += __shfl_sync(kFull, incl, 31);
   }
   __syncwarp();
-  // top-p: keep j while the mass before j is below top_p of the total
+  // top-p: keep j while the mass before j is below top_p of the total; the
+  // masses increase with j, so the kept size is the count of such j.  A cut
+  // whose fixed-point margin is under 2^-17 of the total is redone in double.
   int kp = nsel;
+  bool exact = false;
   if (tp < 1.0f) {
     for (int pass = 0; pass < 2; ++pass) {
-      const double lim = double(tp) * double(W);
-      kp = nsel;
+      const double limd = double(tp) * double(W);
+      const unsigned long long lim = static_cast<unsigned long long>(ceil(limd));
+      int c = 0;
       for (int j0 = 0; j0 < nsel; j0 += 32) {
         const int j = j0 + lane;
-        const uint32_t bal = __ballot_sync(kFull, j < nsel && !(double(ws.before[j]) < lim));
-        if (bal) {
-          kp = j0 + __ffs(bal) - 1;
-          break;
-        }
+        c += __popc(__ballot_sync(kFull, j < nsel && ws.before[j] < lim));
       }
+      kp = c;
       if (pass == 1) break;
-      const double below = kp > 0 ? lim - double(ws.before[kp - 1]) : INFINITY;
-      const double over = kp < nsel ? double(ws.before[kp]) - lim : INFINITY;
-      if (fmin(below, over) >= kToppGuard * double(W)) break;
+      const unsigned long long below = kp > 0 ? lim - ws.before[kp - 1] : ~0ull;
+      const unsigned long long over = kp < nsel ? ws.before[kp] - lim : ~0ull;
+      if (min(below, over) >= (W >> 17)) break;
       // close call: weights and masses in double precision
+      exact = true;
       W = 0ull;
       for (int j0 = 0; j0 < nsel; j0 += 32) {
         const int j = j0 + lane;
         unsigned long long fx = 0ull;
+        double wd = 0.0;
         if (j < nsel) {
-          const double wd = exp((double(composite_value(ws.list[j])) - double(v0)) / double(T));
-          ws.w[j] = wd;
+          wd = exp((double(composite_value(ws.list[j])) - double(v0)) / double(T));
           fx = __double2ull_rn(wd * kFix);
         }
+        __syncwarp();
+        if (j < nsel) ws.wd[j] = wd;
         const unsigned long long incl = warp_incl_scan(fx);
         if (j < nsel) ws.before[j] = W + incl - fx;
         W += __shfl_sync(kFull, incl, 31);
@@ -469,13 +503,20 @@ __device__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, f
   }
   const unsigned long long Wp_fx = kp < nsel ? ws.before[kp] : W;
   const double Wp = double(Wp_fx) / kFix;
-  const double inv = 1.0 / Wp;
+  const double invd = 1.0 / Wp;
+  const float invf = float(invd);
   const size_t cbase = size_t(row) * kTopkMax;
   double pgv = 0.0;
   bool hit = false;
   for (int j = lane; j < kp; j += 32) {
     const int idx = composite_index(ws.list[j]);
-    const double pj = ws.w[j] * inv;
+    double pj;
+    if (exact)
+      pj = ws.wd[j] * invd;
+    else if (ws.we[j] > -100)
+      pj = double(ldexpf(ws.wf[j] * invf, ws.we[j]));
+    else
+      pj = scale2(double(ws.wf[j]), ws.we[j]) * invd;  // far below 2^-100: in double
     w.cand_idx[cbase + j] = idx;
     w.cand_p[cbase + j] = pj;
     if (idx == gx) {
@@ -585,27 +626,35 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
 
 // Final draw of a filtered request from the kept sets, by inverse CDF in
 // vocabulary-index order (double precision): the residual max(0, p - q) over
-// the target's kept tokens after a rejection (a token outside the draft's kept
-// set has q = 0), else p itself.  Run by the warp that finished the request's
-// last row.
-__device__ __noinline__ void decide_filtered(const Problem& P, int b, DrawScratch& ds) {
+// the target's kept tokens of row tr after a rejection (a token outside the
+// draft row dr's kept set has q = 0), else p itself.  One warp; returns the
+// token (warp-uniform).
+__device__ __noinline__ int draw_kept(const Problem& P, int64_t tr, int64_t dr, bool residual,
+                                      double u, DrawScratch& ds) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
-  const int k = P.k_per_req[b];
-  const int t0 = w.t_off[b], d0 = t0 - b;
-  if (__ldcg(&w.req_flag[b])) {
-    fail_request(P, b, k, t0, d0);
-    return;
+  // the first 64 entries of both kept lists are fetched with the kept sizes
+  // (every list slot is addressable; entries past the size are ignored)
+  const int* tidx = w.cand_idx + size_t(tr) * kTopkMax;
+  const double* tpp = w.cand_p + size_t(tr) * kTopkMax;
+  const int* didx = w.cand_idx + size_t(dr) * kTopkMax;
+  const double* dpp = w.cand_p + size_t(dr) * kTopkMax;
+  int tix[2], dix[2] = {0, 0};
+  double tpv[2], dqv[2] = {0.0, 0.0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    tix[h] = __ldcg(tidx + h * 32 + lane);
+    tpv[h] = __ldcg(tpp + h * 32 + lane);
+    if (residual) {
+      dix[h] = __ldcg(didx + h * 32 + lane);
+      dqv[h] = __ldcg(dpp + h * 32 + lane);
+    }
   }
-  const int L = decide(P, b, k, t0, d0, false);
-  const int64_t tr = t0 + L, dr = P.Rt + d0 + L;
-  const bool residual = L < k;
-  const double u = double(P.uniforms[t0 + k]);
   const int Kt = __ldcg(&w.stats[tr].kept);
   const int Kd = residual ? __ldcg(&w.stats[dr].kept) : 0;
   for (int i = lane; i < Kd; i += 32) {
-    ds.idx[i] = __ldcg(&w.cand_idx[size_t(dr) * kTopkMax + i]);
-    ds.v[i] = __ldcg(&w.cand_p[size_t(dr) * kTopkMax + i]);
+    ds.idx[i] = i < 32 ? dix[0] : (i < 64 ? dix[1] : __ldcg(didx + i));
+    ds.v[i] = i < 32 ? dqv[0] : (i < 64 ? dqv[1] : __ldcg(dpp + i));
   }
   const int Psz = max(32, next_pow2(Kt > 0 ? Kt : 1));
   __syncwarp();
@@ -615,8 +664,8 @@ __device__ __noinline__ void decide_filtered(const Problem& P, int b, DrawScratc
     const int j = s * 32 + lane;
     r[s] = 0.0;
     if (j < Kt) {
-      const int idx = __ldcg(&w.cand_idx[size_t(tr) * kTopkMax + j]);
-      const double p = __ldcg(&w.cand_p[size_t(tr) * kTopkMax + j]);
+      const int idx = s == 0 ? tix[0] : (s == 1 ? tix[1] : __ldcg(tidx + j));
+      const double p = s == 0 ? tpv[0] : (s == 1 ? tpv[1] : __ldcg(tpp + j));
       double q = 0.0;
       for (int i = 0; i < Kd; ++i)
         if (ds.idx[i] == idx) q = ds.v[i];
@@ -663,23 +712,90 @@ __device__ __noinline__ void decide_filtered(const Problem& P, int b, DrawScratc
       }
       C = __shfl_sync(kFull, incl, 31);
     }
-    if (lane == 0) P.out_tokens[tr] = y >= 0 ? y : last;
-    break;
+    return y >= 0 ? y : last;
   }
-  __syncwarp();
+  return -1;  // not reached: the second attempt always returns
 }
 
-constexpr int kPostThreads = 256;
+constexpr int kPostThreads = 512;
 constexpr int kWarps = kPostThreads / 32;
+constexpr int kWave = kWarps / 2;  // positions per wave: a target and a draft row each
 
-// Persistent warps over the job list: a filtered row or a decide job, one
-// warp each.  The warp that completes a filtered request's last row decides it.
+struct PostShared {
+  int L;
+};
+
+// A filtered request, by one CTA, in waves of kWave positions: warps 2j and
+// 2j + 1 filter the target and draft rows of position w0 + j, the first spare
+// warp of the wave that reaches position k - 1 filters the bonus row k, then
+// warp 0 decides the wave's positions in order.  Verification stops at the
+// first rejection, so rows past it are never filtered.  (p, q) are reported
+// for the positions up to the stop, NaN after it.
 template <bool BF16>
-__global__ void __launch_bounds__(kPostThreads, 4) filter_decide_kernel(const Problem P) {
-  extern __shared__ __align__(16) unsigned char post_smem[];
-  WarpScratch& ws = reinterpret_cast<WarpScratch*>(post_smem)[threadIdx.x >> 5];
+__device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScratch* scr,
+                                 PostShared& sh) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int d0 = t0 - b;
+  const int K = P.top_k[b];
+  const float T = P.temperature[b];
+  const float tp = P.top_p ? P.top_p[b] : 1.0f;
+  for (int w0 = 0;; w0 += kWave) {
+    const int pos = w0 + (warp >> 1);
+    if (pos < k) {
+      const int64_t row = (warp & 1) ? P.Rt + d0 + pos : int64_t(t0) + pos;
+      warp_filter_row<BF16>(P, row, K, T, tp, P.draft_tokens[d0 + pos], scr[warp].sel);
+    } else if (warp == 2 * max(k - w0, 0)) {
+      warp_filter_row<BF16>(P, t0 + k, K, T, tp, -1, scr[warp].sel);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int L = k;  // k == 0: only the bonus row
+      if (w0 < k) {
+        const int n = min(kWave, k - w0);
+        bool acc = true;
+        double p = 0.0, q = 0.0;
+        if (lane < n) {
+          p = w.stats[t0 + w0 + lane].pg;
+          q = w.stats[P.Rt + d0 + w0 + lane].pg;
+          acc = double(P.uniforms[t0 + w0 + lane]) < p / q;
+        }
+        const uint32_t rej = __ballot_sync(kFull, lane < n && !acc);
+        L = rej ? w0 + __ffs(rej) - 1 : (w0 + n == k ? k : -1);  // -1: carry on
+        if (P.out_pq && lane < n && (L < 0 || w0 + lane <= L)) {
+          P.out_pq[2 * int64_t(d0 + w0 + lane)] = p;
+          P.out_pq[2 * int64_t(d0 + w0 + lane) + 1] = q;
+        }
+      }
+      if (lane == 0) sh.L = L;
+    }
+    __syncthreads();
+    if (sh.L >= 0) break;
+  }
+  const int L = sh.L;
+  if (warp == 0) {
+    const int y = draw_kept(P, t0 + L, P.Rt + d0 + L, L < k, double(P.uniforms[t0 + k]),
+                            scr[0].draw);
+    for (int i = lane; i <= k; i += 32)
+      P.out_tokens[t0 + i] = i < L ? P.draft_tokens[d0 + i] : (i == L ? y : -1);
+    if (P.out_pq)
+      for (int i = L + 1 + lane; i < k; i += 32) {
+        P.out_pq[2 * int64_t(d0 + i)] = nan64();
+        P.out_pq[2 * int64_t(d0 + i) + 1] = nan64();
+      }
+    if (lane == 0) P.out_accept_len[b] = L;
+  }
+}
+
+// Persistent CTAs over the job lists: a filtered request takes a whole CTA;
+// the other requests are decided kWarps at a time, one warp each.
+template <bool BF16>
+__global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Problem P) {
+  extern __shared__ __align__(16) unsigned char post_smem[];
+  WarpScratch* scr = reinterpret_cast<WarpScratch*>(post_smem);
+  __shared__ PostShared sh;
+  const Ws& w = P.ws;
+  const int warp = threadIdx.x >> 5;
   if (w.hdr->global_err) {
     // batch-level data error: every output is -1 (NaN for the probabilities)
     const int64_t stride = int64_t(gridDim.x) * kPostThreads;
@@ -690,26 +806,20 @@ __global__ void __launch_bounds__(kPostThreads, 4) filter_decide_kernel(const Pr
       for (int64_t r = i0; r < 2 * P.Rd; r += stride) P.out_pq[r] = nan64();
     return;
   }
-  const int njobs = w.hdr->n_jobs;
-  for (int j = blockIdx.x * kWarps + warp; j < njobs; j += gridDim.x * kWarps) {
-    const int4 job = w.job[j];
-    const int b = job.x;
-    if (job.y < 0) {
-      decide_request(P, b);
-      continue;
-    }
-    const int k = P.k_per_req[b];
-    if (!w.req_flag[b])
-      warp_filter_row<BF16>(P, job.z, P.top_k[b], P.temperature[b],
-                            P.top_p ? P.top_p[b] : 1.0f, job.w, ws.sel);
-    __threadfence();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&w.req_cnt[b], 1) == 2 * k;
-    last = __shfl_sync(kFull, last, 0);
-    if (last) {
-      __threadfence();
-      decide_filtered(P, b, ws.draw);
+  const int nf = w.hdr->n_filtered, nd = w.hdr->n_decide;
+  const int units = nf + (nd + kWarps - 1) / kWarps;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    if (u < nf) {
+      const int4 job = w.job[u];
+      if (w.req_flag[job.x]) {  // a logit error found by the row pass
+        if (warp == 0) fail_request(P, job.x, job.w, job.z, job.z - job.x);
+      } else {
+        filtered_request<BF16>(P, job.x, job.z, job.w, scr, sh);
+      }
+      __syncthreads();  // the scratch is reused by the next unit
+    } else {
+      const int j = (u - nf) * kWarps + warp;
+      if (j < nd) decide_request(P, w.job[P.B + j].x);
     }
   }
 }

@@ -35,9 +35,10 @@ struct WsHeader {
   int64_t err_row;
   int32_t n_active;     // rows the row pass must stream
   int32_t global_err;   // batch-level data error (row counts)
-  int32_t n_jobs;       // filter / decide jobs listed by the setup kernel
+  int32_t n_filtered;   // filtered requests listed by the setup kernel
+  int32_t n_decide;     // other requests listed by the setup kernel
   int32_t n_draw;       // requests queued for the unfiltered draw
-  int32_t pad[8];
+  int32_t pad[7];
 };
 
 struct RowStat {
@@ -69,15 +70,14 @@ struct Ws {
   int32_t* cand_idx; // [R, kTopkMax]
   double* cand_p;    // [R, kTopkMax]
   uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys)
-  int4* job;          // [R] {request, row i of the request (0..2k) or -1 for a
-                      //      decide job, logit row, the row's draft token or -1}
-  int32_t* req_cnt;   // [B] filtered rows finished
+  int4* job;          // [2B] {request, 0, t_off, k}: filtered requests from 0,
+                      //      the other requests from B
   DrawDesc* draw;     // [B] queued draws, in queue order
 };
 
 struct WsLayout {
   size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, off_raw, off_job,
-      off_rcnt, off_draw, total;
+      off_draw, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -94,8 +94,7 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   L.off_cp = o;      o = align256(o + sizeof(double) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_raw = o;     o = align256(o + sizeof(uint64_t) * kRawCap * (size_t)(R > 0 ? R : 1));
   const size_t B1 = (size_t)(B > 0 ? B : 1);
-  L.off_job = o;     o = align256(o + sizeof(int4) * (size_t)(R > 0 ? R : 1));
-  L.off_rcnt = o;    o = align256(o + sizeof(int32_t) * B1);
+  L.off_job = o;     o = align256(o + sizeof(int4) * 2 * B1);
   L.off_draw = o;    o = align256(o + sizeof(DrawDesc) * B1);
   L.total = o;
   return L;
@@ -113,7 +112,6 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.cand_p = reinterpret_cast<double*>(p + L.off_cp);
   w.cand_raw = reinterpret_cast<uint64_t*>(p + L.off_raw);
   w.job = reinterpret_cast<int4*>(p + L.off_job);
-  w.req_cnt = reinterpret_cast<int32_t*>(p + L.off_rcnt);
   w.draw = reinterpret_cast<DrawDesc*>(p + L.off_draw);
   return w;
 }

@@ -47,7 +47,8 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     w.hdr->err_row = -1;
     w.hdr->n_active = 0;
     w.hdr->global_err = 0;
-    w.hdr->n_jobs = 0;
+    w.hdr->n_filtered = 0;
+    w.hdr->n_decide = 0;
     w.hdr->n_draw = 0;
     s_bad = 0;
   }
@@ -85,9 +86,8 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   if (s_bad) return;
 
   // Pass 2: per-request validation, modes, the active row list and the
-  // post-pass job list (2k + 1 filter jobs for a filtered request, one decide
-  // job for any other).
-  int carry_a = 0, carry_j = 0;
+  // post-pass job lists (filtered requests; all others).
+  int carry_a = 0, carry_f = 0, carry_o = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int code = 0, active = 0, mode_t = kSkip, mode_d = kSkip, k = 0, t0 = 0, d0 = 0;
@@ -125,22 +125,18 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       }
     }
     const bool filt = !code && mode_t == kTopk;
-    const int njob = b < P.B ? (filt ? 2 * k + 1 : 1) : 0;
-    int tot, totj;
+    int tot, totf, toto;
     const int a0 = carry_a + block_exclusive_scan(active, &tot);
     carry_a += tot;
-    const int j0 = carry_j + block_exclusive_scan(njob, &totj);
-    carry_j += totj;
+    const int f0 = carry_f + block_exclusive_scan(b < P.B && filt ? 1 : 0, &totf);
+    carry_f += totf;
+    const int o0 = carry_o + block_exclusive_scan(b < P.B && !filt ? 1 : 0, &toto);
+    carry_o += toto;
     if (b < P.B) {
-      if (filt) {
-        for (int i = 0; i <= k; ++i)
-          w.job[j0 + i] = make_int4(b, i, t0 + i, i < k ? P.draft_tokens[d0 + i] : -1);
-        for (int i = 0; i < k; ++i)
-          w.job[j0 + k + 1 + i] = make_int4(b, k + 1 + i, int(P.Rt) + d0 + i, P.draft_tokens[d0 + i]);
-      } else {
-        w.job[j0] = make_int4(b, -1, 0, -1);
-      }
-      w.req_cnt[b] = 0;
+      if (filt)
+        w.job[f0] = make_int4(b, 0, t0, k);
+      else
+        w.job[P.B + o0] = make_int4(b, 0, t0, k);
     }
     if (b < P.B && active) {
       int a = a0;
@@ -168,7 +164,8 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   }
   if (threadIdx.x == 0) {
     w.hdr->n_active = carry_a;
-    w.hdr->n_jobs = carry_j;
+    w.hdr->n_filtered = carry_f;
+    w.hdr->n_decide = carry_o;
   }
 }
 

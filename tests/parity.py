@@ -8,7 +8,8 @@ margin < 1e-5 (the tolerances of the verification path), or top-p decision
 margin < 1e-12 (both sides take that decision in double precision).  Those
 requests are counted and reported; every request must still be structurally
 valid.  p_i(x_i) and q_i(x_i) must match within 1e-5 relative for float32
-logits and 2e-3 for bfloat16 logits.
+logits and 2e-3 for bfloat16 logits at every position the decision examined
+(up to the first rejection).
 """
 
 from __future__ import annotations
@@ -96,8 +97,12 @@ def compare(batch_cpu, g, o, name=""):
                 rep.structural.append(b)
     if g["pq"] is not None and batch_cpu.draft_rows:
         tol = PQ_RTOL[batch_cpu.target.dtype]
-        rows = np.concatenate([np.arange(d_off[b], d_off[b] + k[b]) for b in range(B)
-                               if T[b] > 0 and o["accept_len"][b] >= 0] or [np.zeros(0, int)])
+        # positions the decision examined: 0 .. min(L, k - 1); the library may
+        # leave later positions unevaluated (NaN)
+        rows = np.concatenate([np.arange(d_off[b], d_off[b] + min(int(g["acc"][b]) + 1, k[b]))
+                               for b in range(B)
+                               if T[b] > 0 and o["accept_len"][b] >= 0 and g["acc"][b] >= 0]
+                              or [np.zeros(0, int)])
         if len(rows):
             gp, op = g["pq"][rows], o["pq"][rows]
             pos = op > 0

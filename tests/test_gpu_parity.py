@@ -99,11 +99,22 @@ def test_softmax_statistics_match_torch_logsumexp():
 def test_filtered_kept_sets_match_oracle():
     batch = W.make_batch("c4", device=DEV, batch=16)
     v = sv.Verifier(DEV)
-    run_gpu(batch, v)
+    g = run_gpu(batch, v)
     B, Rt, Rd = batch.batch, batch.target_rows, batch.draft_rows
     d = v.dump(B, Rt, Rd)
     rows = torch.cat([batch.target, batch.draft]).cpu()
-    for r in range(0, Rt + Rd, 7):
+    # rows the verification needed: positions up to the first rejection (the
+    # bonus row after k acceptances); later rows are never filtered
+    acc = g["acc"]
+    k = batch.k_per_req.cpu().numpy()
+    t_off = t_offsets(k)
+    needed = []
+    for b in range(B):
+        L = int(acc[b])
+        needed += [t_off[b] + i for i in range(L + 1)]
+        needed += [Rt + t_off[b] - b + i for i in range(min(L + 1, k[b]))]
+    assert len(needed) > 0
+    for r in needed:
         p, _ = oracle.row_probs(rows[r], 1.0, 50, 0.9)
         nz = np.nonzero(p)[0]
         n = int(d["kept_count"][r])
