@@ -105,14 +105,16 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       else if (tk < 0) code = SV_ERR_DATA_TOP_K;
       else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
       else if (T > 0.0f && k > 0 && P.draft == nullptr) code = SV_ERR_DATA_NO_DRAFT;
-      if (!code)
+      if (!code) {
+        // no early exit: the (at most SV_MAX_K) loads are independent
+        bool bad = false;
+#pragma unroll 8
         for (int i = 0; i < k; ++i) {
           const int x = P.draft_tokens[d0 + i];
-          if (x < 0 || x >= P.V) {
-            code = SV_ERR_DATA_TOKEN;
-            break;
-          }
+          bad |= x < 0 || x >= P.V;
         }
+        if (bad) code = SV_ERR_DATA_TOKEN;
+      }
       w.req_flag[b] = code;
       if (code) {
         record_error(w.hdr, code, b, -1);
