@@ -869,8 +869,9 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       // ---- fast path: speculative threshold, one sweep
       {
         const int e0 = tail_start < kTileElems ? tail_start : kTileElems;  // elements in tile 0
-        const double lam = double(K) * double(e0) / double(P.V);
-        const int r = int(ceil(lam + 4.0 * sqrt(lam) + 4.0));
+        // float arithmetic: r is a safety margin, and the FP64 pipe is narrow
+        const float lam = float(K) * float(e0) / float(P.V);
+        const int r = int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f));
         const int L = (2 * r + kConsumerWarps - 1) / kConsumerWarps;
         for (int t = 0; t < ntiles; ++t) {
           const uint4* tile = acquire();
