@@ -196,9 +196,13 @@ int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t
   if (kept_idx && cudaMemcpy(kept_idx, base + L.off_cidx, R * kTopkMax * sizeof(int32_t),
                              cudaMemcpyDeviceToHost) != cudaSuccess)
     return SV_ERR_CUDA;
-  if (kept_p && cudaMemcpy(kept_p, base + L.off_cp, R * kTopkMax * sizeof(double),
-                           cudaMemcpyDeviceToHost) != cudaSuccess)
-    return SV_ERR_CUDA;
+  if (kept_p) {
+    std::vector<float> kp(R * kTopkMax);
+    if (cudaMemcpy(kp.data(), base + L.off_cp, R * kTopkMax * sizeof(float),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      return SV_ERR_CUDA;
+    for (size_t i = 0; i < kp.size(); ++i) kept_p[i] = kp[i];
+  }
   return SV_OK;
 }
 

@@ -438,8 +438,16 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   sort_desc(ws.list, Psz);
 
   const float v0 = composite_value(ws.list[0]);
-  const double cd = 1.4426950408889634 / double(T);
-  const float chi = float(cd), clo = float(cd - double(chi));
+  // log2(e) / T split into two floats, formed once per row (the FP64 pipe is
+  // narrow: per-lane double work would queue on it)
+  float chi = 0.f, clo = 0.f;
+  if (lane == 0) {
+    const double cd = 1.4426950408889634 / double(T);
+    chi = float(cd);
+    clo = float(cd - double(chi));
+  }
+  chi = __shfl_sync(kFull, chi, 0);
+  clo = __shfl_sync(kFull, clo, 0);
   // weights and the fixed-point mass before each j (integer work; the FP64
   // pipe, scarce on this part, is kept for a few operations per row)
   unsigned long long W = 0ull;
@@ -469,8 +477,9 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   bool exact = false;
   if (tp < 1.0f) {
     for (int pass = 0; pass < 2; ++pass) {
-      const double limd = double(tp) * double(W);
-      const unsigned long long lim = static_cast<unsigned long long>(ceil(limd));
+      unsigned long long lim = 0ull;
+      if (lane == 0) lim = static_cast<unsigned long long>(ceil(double(tp) * double(W)));
+      lim = __shfl_sync(kFull, lim, 0);
       int c = 0;
       for (int j0 = 0; j0 < nsel; j0 += 32) {
         const int j = j0 + lane;
@@ -502,21 +511,25 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
     }
   }
   const unsigned long long Wp_fx = kp < nsel ? ws.before[kp] : W;
-  const double Wp = double(Wp_fx) / kFix;
-  const double invd = 1.0 / Wp;
+  double Wp = 0.0, invd = 0.0;
+  if (lane == 0) {
+    Wp = double(Wp_fx) / kFix;
+    invd = 1.0 / Wp;
+  }
+  invd = __shfl_sync(kFull, invd, 0);
   const float invf = float(invd);
   const size_t cbase = size_t(row) * kTopkMax;
-  double pgv = 0.0;
+  float pgv = 0.f;
   bool hit = false;
   for (int j = lane; j < kp; j += 32) {
     const int idx = composite_index(ws.list[j]);
-    double pj;
+    float pj;
     if (exact)
-      pj = ws.wd[j] * invd;
+      pj = float(ws.wd[j] * invd);
     else if (ws.we[j] > -100)
-      pj = double(ldexpf(ws.wf[j] * invf, ws.we[j]));
+      pj = ws.wf[j] * invf * __int_as_float((ws.we[j] + 127) << 23);
     else
-      pj = scale2(double(ws.wf[j]), ws.we[j]) * invd;  // far below 2^-100: in double
+      pj = float(scale2(double(ws.wf[j]), ws.we[j]) * invd);  // far below 2^-100: in double
     w.cand_idx[cbase + j] = idx;
     w.cand_p[cbase + j] = pj;
     if (idx == gx) {
@@ -559,7 +572,7 @@ __device__ int decide(const Problem& P, int b, int k, int t0, int d0, bool greed
     } else {
       const double p = __ldcg(&w.stats[t0 + lane].pg);
       const double q = __ldcg(&w.stats[P.Rt + d0 + lane].pg);
-      acc = double(P.uniforms[t0 + lane]) < p / q;
+      acc = double(P.uniforms[t0 + lane]) * q < p;  // u < p / q without a divide
       if (P.out_pq) {
         P.out_pq[2 * int64_t(d0 + lane)] = p;
         P.out_pq[2 * int64_t(d0 + lane) + 1] = q;
@@ -636,11 +649,11 @@ __device__ __noinline__ int draw_kept(const Problem& P, int64_t tr, int64_t dr, 
   // the first 64 entries of both kept lists are fetched with the kept sizes
   // (every list slot is addressable; entries past the size are ignored)
   const int* tidx = w.cand_idx + size_t(tr) * kTopkMax;
-  const double* tpp = w.cand_p + size_t(tr) * kTopkMax;
+  const float* tpp = w.cand_p + size_t(tr) * kTopkMax;
   const int* didx = w.cand_idx + size_t(dr) * kTopkMax;
-  const double* dpp = w.cand_p + size_t(dr) * kTopkMax;
+  const float* dpp = w.cand_p + size_t(dr) * kTopkMax;
   int tix[2], dix[2] = {0, 0};
-  double tpv[2], dqv[2] = {0.0, 0.0};
+  float tpv[2], dqv[2] = {0.f, 0.f};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     tix[h] = __ldcg(tidx + h * 32 + lane);
@@ -758,7 +771,7 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
         if (lane < n) {
           p = w.stats[t0 + w0 + lane].pg;
           q = w.stats[P.Rt + d0 + w0 + lane].pg;
-          acc = double(P.uniforms[t0 + w0 + lane]) < p / q;
+          acc = double(P.uniforms[t0 + w0 + lane]) * q < p;  // u < p / q
         }
         const uint32_t rej = __ballot_sync(kFull, lane < n && !acc);
         L = rej ? w0 + __ffs(rej) - 1 : (w0 + n == k ? k : -1);  // -1: carry on

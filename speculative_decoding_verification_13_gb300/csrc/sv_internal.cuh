@@ -68,7 +68,7 @@ struct Ws {
   int4* rowlist;     // [R] {row, request, gather token, (pos << 2) | mode}
   RowStat* stats;    // [R]
   int32_t* cand_idx; // [R, kTopkMax]
-  double* cand_p;    // [R, kTopkMax]
+  float* cand_p;     // [R, kTopkMax] kept probabilities
   uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys)
   int4* job;          // [2B] {request, 0, t_off, k}: filtered requests from 0,
                       //      the other requests from B
@@ -91,7 +91,7 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   L.off_rowlist = o; o = align256(o + sizeof(int4) * (size_t)(R > 0 ? R : 1));
   L.off_stats = o;   o = align256(o + sizeof(RowStat) * (size_t)(R > 0 ? R : 1));
   L.off_cidx = o;    o = align256(o + sizeof(int32_t) * kTopkMax * (size_t)(R > 0 ? R : 1));
-  L.off_cp = o;      o = align256(o + sizeof(double) * kTopkMax * (size_t)(R > 0 ? R : 1));
+  L.off_cp = o;      o = align256(o + sizeof(float) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_raw = o;     o = align256(o + sizeof(uint64_t) * kRawCap * (size_t)(R > 0 ? R : 1));
   const size_t B1 = (size_t)(B > 0 ? B : 1);
   L.off_job = o;     o = align256(o + sizeof(int4) * 2 * B1);
@@ -109,7 +109,7 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.rowlist = reinterpret_cast<int4*>(p + L.off_rowlist);
   w.stats = reinterpret_cast<RowStat*>(p + L.off_stats);
   w.cand_idx = reinterpret_cast<int32_t*>(p + L.off_cidx);
-  w.cand_p = reinterpret_cast<double*>(p + L.off_cp);
+  w.cand_p = reinterpret_cast<float*>(p + L.off_cp);
   w.cand_raw = reinterpret_cast<uint64_t*>(p + L.off_raw);
   w.job = reinterpret_cast<int4*>(p + L.off_job);
   w.draw = reinterpret_cast<DrawDesc*>(p + L.off_draw);
