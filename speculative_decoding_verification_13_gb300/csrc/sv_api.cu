@@ -3,6 +3,7 @@
 // caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -148,8 +149,11 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   const int64_t fmax = int64_t(sms) * ds.occ_filter;
   if (launch_filter_decide(P, bf16, int(fjobs < fmax ? fjobs : fmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
-  const int64_t djobs = batch;  // at most one queued draw per request
+  // draw pass: a queued draw is cut into segments when there are few requests,
+  // so that every SM streams (at most one queued draw per request)
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
+  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, dmax / std::max(batch, 1))));
+  const int64_t djobs = int64_t(batch) * P.n_seg;
   if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;

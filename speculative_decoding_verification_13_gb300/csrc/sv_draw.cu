@@ -103,6 +103,7 @@ struct DrawPassShared {
   double R;
   int tstar;
   int fallback;
+  int last;
   int cabort;
   int pabort;
 };
@@ -144,7 +145,7 @@ __device__ __forceinline__ float warp_scan_f(float v) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
+__global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P) {
   using E = Elt<BF16>;
   constexpr int kEPS = kDHalf / E::kSize;  // elements of a row per stage
   constexpr int kTPS = kEPS / kDTile;      // tiles per stage
@@ -172,6 +173,19 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
   const int64_t bulk = (int64_t(V) * E::kSize) & ~int64_t(15);
   const int nst = int((bulk + kDHalf - 1) / kDHalf);
   const int fast_end = int(bulk / E::kSize);  // elements the bulk copies deliver
+  // Each queued draw is cut into nseg segments of whole stages (the last one
+  // also owns the tiles past the bulk-copied part); a unit is one segment.
+  const int nseg = max(1, min(P.n_seg, nst));
+  const int sps = nst > 0 ? (nst + nseg - 1) / nseg : 0;  // stages per segment
+  const int units = n_draw * nseg;
+  auto seg_stages = [&](int s, int* a, int* z) {
+    *a = min(nst, s * sps);
+    *z = min(nst, (s + 1) * sps);
+  };
+  auto seg_tiles = [&](int s, int* a, int* z) {
+    *a = min(ntile, s * sps * kTPS);
+    *z = s == nseg - 1 ? ntile : min(ntile, (s + 1) * sps * kTPS);
+  };
 
   // ------------------------------------------------------------- producer
   if (warp == 0) {
@@ -179,13 +193,16 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
     bool stop = false;
-    for (int q = blockIdx.x; q < n_draw && !stop; q += gridDim.x) {
+    for (int u = blockIdx.x; u < units && !stop; u += gridDim.x) {
+      const int q = u / nseg, sg = u - q * nseg;
       const DrawDesc d = w.draw[q];
       const char* tsrc = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
       const char* dsrc = d.kind == 1 ? static_cast<const char*>(P.draft) +
                                            (d.dr - P.Rt) * P.d_stride * E::kSize
                                      : nullptr;
-      for (int s = 0; s < nst; ++s) {
+      int sa, sz;
+      seg_stages(sg, &sa, &sz);
+      for (int s = sa; s < sz; ++s) {
         const int64_t rem = bulk - int64_t(s) * kDHalf;
         const uint32_t bytes = uint32_t(rem < kDHalf ? rem : kDHalf);
         if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
@@ -221,7 +238,28 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
   // ------------------------------------------------------------- consumers
   const int cwarp = warp - 1;
   uint32_t stage = 0, phase = 0;
-  for (int q = blockIdx.x; q < n_draw; q += gridDim.x) {
+  // tile sum of tile tau read from global memory, with weights W
+  auto tile_from_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau) {
+    const int e = tau * kDTile + lane * 8;
+    float xt[8], xd[8];
+    elems8<BF16>(nullptr, trow, e, 0, V, xt);
+    if (Wt.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
+    float ls = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ls += Wt(xt[k], Wt.kind == 1 ? xd[k] : 0.f);
+    return __shfl_sync(kFull, warp_scan_f(ls), 31);
+  };
+  // sum of tiles [a, z) in tile order (double), one warp
+  auto tiles_total = [&](int a, int z) {
+    double tot = 0.0;
+    for (int t0 = a; t0 < z; t0 += 32) {
+      const double v = t0 + lane < z ? double(ts[t0 + lane]) : 0.0;
+      tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
+    }
+    return tot;
+  };
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int q = u / nseg, sg = u - q * nseg;
     const DrawDesc d = w.draw[q];
     Weights W;
     W.mt = d.mt;
@@ -234,8 +272,11 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
     const void* drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
                                          (d.dr - P.Rt) * P.d_stride * E::kSize
                                    : nullptr;
-    // tile sums: the tiles of each stage as it lands
-    for (int s = 0; s < nst; ++s) {
+    int sa, sz, ta, tz;
+    seg_stages(sg, &sa, &sz);
+    seg_tiles(sg, &ta, &tz);
+    // tile sums of this segment: the tiles of each stage as it lands
+    for (int s = sa; s < sz; ++s) {
       if (!wait_bar(full0 + 8u * stage, phase, &S.cabort, &S.pabort, 16)) {
         *reinterpret_cast<volatile int*>(&S.cabort) = 1;
         record_error(w.hdr, SV_ERR_TIMEOUT, -1, d.tr);
@@ -264,26 +305,36 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
         phase ^= 1u;
       }
     }
-    // tiles past the bulk-copied part of the row, from global memory
-    for (int tau = nst * kTPS + cwarp; tau < ntile; tau += kDConsumerWarps) {
-      const int e = tau * kDTile + lane * 8;
-      float xt[8], xd[8];
-      elems8<BF16>(nullptr, trow, e, 0, V, xt);
-      if (W.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
-      float ls = 0.f;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
-      const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
+    // tiles past the bulk-copied part of the row (last segment), from global memory
+    for (int tau = max(ta, nst * kTPS) + cwarp; tau < tz; tau += kDConsumerWarps) {
+      const float tsum = tile_from_global(W, trow, drow, tau);
       if (lane == 0) ts[tau] = tsum;
     }
     draw_sync();
     if (*reinterpret_cast<volatile int*>(&S.cabort)) break;
-    // total S, in tile order
+    // the segment's sum; the CTA that completes a draw's last segment locates it
     if (cwarp == 0) {
-      double tot = 0.0;
-      for (int t0 = 0; t0 < ntile; t0 += 32) {
-        const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
-        tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
+      const double segsum = tiles_total(ta, tz);
+      int last = 1;
+      if (nseg > 1 && lane == 0) {
+        w.seg_sum[size_t(q) * kMaxSeg + sg] = segsum;
+        __threadfence();
+        last = atomicAdd(&w.seg_cnt[q], 1) == nseg - 1;
+      }
+      if (lane == 0) {
+        S.last = last;
+        S.S = segsum;
+      }
+    }
+    draw_sync();
+    if (!S.last) continue;
+    if (nseg > 1) __threadfence();  // the other segments' sums are read below
+    // total S over the segments, in segment order (one warp)
+    if (cwarp == 0) {
+      double tot = S.S;
+      if (nseg > 1) {
+        const double v = lane < nseg ? __ldcg(&w.seg_sum[size_t(q) * kMaxSeg + lane]) : 0.0;
+        tot = __shfl_sync(kFull, warp_scan_d(v), 31);
       }
       if (lane == 0) {
         S.S = tot;
@@ -291,42 +342,68 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
       }
     }
     draw_sync();
+    int nsegL = nseg;  // segments of the sums the search below walks
     if (S.fallback) {
-      // residual mass vanished through rounding: draw from p_L
+      // residual mass vanished through rounding: draw from p_L, every tile again
       W.kind = 2;
       for (int tau = cwarp; tau < ntile; tau += kDConsumerWarps) {
-        const int e = tau * kDTile + lane * 8;
-        float xt[8];
-        elems8<BF16>(nullptr, trow, e, 0, V, xt);
-        float ls = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ls += W(xt[k], 0.f);
-        const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
+        const float tsum = tile_from_global(W, trow, drow, tau);
         if (lane == 0) ts[tau] = tsum;
       }
       draw_sync();
       if (cwarp == 0) {
-        double tot = 0.0;
-        for (int t0 = 0; t0 < ntile; t0 += 32) {
-          const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
-          tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
-        }
+        const double tot = tiles_total(0, ntile);
         if (lane == 0) S.S = tot;
       }
+      nsegL = 1;
       draw_sync();
+    }
+    const double t = d.u * S.S;
+    // the segment whose inclusive prefix first exceeds t (R: the prefix before it)
+    if (cwarp == 0) {
+      int sstar = 0;
+      double R = 0.0;
+      if (nsegL > 1) {
+        const double v = lane < nseg ? __ldcg(&w.seg_sum[size_t(q) * kMaxSeg + lane]) : 0.0;
+        const double incl = warp_scan_d(v);
+        double ex = __shfl_up_sync(kFull, incl, 1);
+        if (lane == 0) ex = 0.0;
+        const uint32_t hit = __ballot_sync(kFull, lane < nseg && incl > t);
+        const uint32_t pos = __ballot_sync(kFull, lane < nseg && v > 0.0);
+        const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : nseg - 1);
+        sstar = l;
+        R = __shfl_sync(kFull, ex, l);
+      }
+      if (lane == 0) {
+        S.tstar = sstar;
+        S.R = R;
+      }
+    }
+    draw_sync();
+    const int sstar = S.tstar;
+    int sa2 = 0, sz2 = ntile;
+    if (nsegL > 1) {
+      seg_tiles(sstar, &sa2, &sz2);
+      if (sstar != sg) {
+        // that segment's tile sums, recomputed from global memory (L2)
+        for (int tau = sa2 + cwarp; tau < sz2; tau += kDConsumerWarps) {
+          const float tsum = tile_from_global(W, trow, drow, tau);
+          if (lane == 0) ts[tau] = tsum;
+        }
+        draw_sync();
+      }
     }
     if (cwarp == 0) {
       // the tile where the prefix first exceeds t, then the element in it
-      const double t = d.u * S.S;
-      double carry = 0.0, R = 0.0, Rlast = 0.0;
+      double carry = S.R, R = S.R, Rlast = S.R;
       int tstar = -1, tlast = -1;
-      for (int t0 = 0; t0 < ntile && tstar < 0; t0 += 32) {
-        const double v = t0 + lane < ntile ? double(ts[t0 + lane]) : 0.0;
+      for (int t0 = sa2; t0 < sz2 && tstar < 0; t0 += 32) {
+        const double v = t0 + lane < sz2 ? double(ts[t0 + lane]) : 0.0;
         const double incl = warp_scan_d(v) + carry;
         double ex = __shfl_up_sync(kFull, incl, 1);
         if (lane == 0) ex = carry;
         const uint32_t pos = __ballot_sync(kFull, v > 0.0);
-        const uint32_t hit = __ballot_sync(kFull, t0 + lane < ntile && incl > t);
+        const uint32_t hit = __ballot_sync(kFull, t0 + lane < sz2 && incl > t);
         if (pos) {
           const int l = 31 - __clz(pos);
           tlast = t0 + l;
@@ -378,7 +455,7 @@ __global__ void __launch_bounds__(kDThreads) draw_pass_kernel(const Problem P) {
         P.out_tokens[d.t0 + d.L] = y;
       }
     }
-    draw_sync();  // tile sums are rewritten by the next request
+    draw_sync();  // tile sums are rewritten by the next unit
   }
 }
 

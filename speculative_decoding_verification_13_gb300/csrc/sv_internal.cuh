@@ -24,6 +24,7 @@ constexpr int kRawCap = 1024;                            // top-k survivors kept
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
+constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
 
 // Row modes chosen per request by the setup kernel.
 enum RowMode : int { kSkip = 0, kStats = 1, kArgmax = 2, kTopk = 3 };
@@ -73,11 +74,13 @@ struct Ws {
   int4* job;          // [2B] {request, 0, t_off, k}: filtered requests from 0,
                       //      the other requests from B
   DrawDesc* draw;     // [B] queued draws, in queue order
+  double* seg_sum;    // [B, kMaxSeg] weight sum of each segment of a queued draw
+  int32_t* seg_cnt;   // [B] segments of a queued draw finished
 };
 
 struct WsLayout {
   size_t off_t_off, off_flag, off_rowlist, off_stats, off_cidx, off_cp, off_raw, off_job,
-      off_draw, total;
+      off_draw, off_seg, off_scnt, total;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -96,6 +99,8 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   const size_t B1 = (size_t)(B > 0 ? B : 1);
   L.off_job = o;     o = align256(o + sizeof(int4) * 2 * B1);
   L.off_draw = o;    o = align256(o + sizeof(DrawDesc) * B1);
+  L.off_seg = o;     o = align256(o + sizeof(double) * kMaxSeg * B1);
+  L.off_scnt = o;    o = align256(o + sizeof(int32_t) * B1);
   L.total = o;
   return L;
 }
@@ -113,6 +118,8 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.cand_raw = reinterpret_cast<uint64_t*>(p + L.off_raw);
   w.job = reinterpret_cast<int4*>(p + L.off_job);
   w.draw = reinterpret_cast<DrawDesc*>(p + L.off_draw);
+  w.seg_sum = reinterpret_cast<double*>(p + L.off_seg);
+  w.seg_cnt = reinterpret_cast<int32_t*>(p + L.off_scnt);
   return w;
 }
 
@@ -124,6 +131,7 @@ struct Problem {
   int64_t Rt, Rd;
   int32_t V;
   int32_t B;
+  int32_t n_seg;                // draw-pass segments per queued draw (1..kMaxSeg)
   const int32_t* draft_tokens;
   const int32_t* k_per_req;
   const float* temperature;

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     const int o0 = carry_o + block_exclusive_scan(b < P.B && !filt ? 1 : 0, &toto);
     carry_o += toto;
     if (b < P.B) {
+      w.seg_cnt[b] = 0;
       if (filt)
         w.job[f0] = make_int4(b, 0, t0, k);
       else
