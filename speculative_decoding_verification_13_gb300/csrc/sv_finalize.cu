@@ -663,8 +663,8 @@ __device__ __noinline__ int draw_kept(const Problem& P, int64_t tr, int64_t dr, 
       dqv[h] = __ldcg(dpp + h * 32 + lane);
     }
   }
-  const int Kt = __ldcg(&w.stats[tr].kept);
-  const int Kd = residual ? __ldcg(&w.stats[dr].kept) : 0;
+  const int Kt = min(max(__ldcg(&w.stats[tr].kept), 0), kTopkMax);
+  const int Kd = residual ? min(max(__ldcg(&w.stats[dr].kept), 0), kTopkMax) : 0;
   for (int i = lane; i < Kd; i += 32) {
     ds.idx[i] = i < 32 ? dix[0] : (i < 64 ? dix[1] : __ldcg(didx + i));
     ds.v[i] = i < 32 ? dqv[0] : (i < 64 ? dqv[1] : __ldcg(dpp + i));
@@ -740,8 +740,9 @@ struct PostShared {
 
 // A filtered request, by one CTA, in waves of kWave positions: warps 2j and
 // 2j + 1 filter the target and draft rows of position w0 + j, the first spare
-// warp of the wave that reaches position k - 1 filters the bonus row k, then
-// warp 0 decides the wave's positions in order.  Verification stops at the
+// warp of the wave that reaches position k - 1 filters the bonus row k (when
+// that wave fills every warp, k a multiple of kWave, warp 0 of one more wave
+// does), then warp 0 decides the wave's positions in order.  Verification stops at the
 // first rejection, so rows past it are never filtered.  (p, q) are reported
 // for the positions up to the stop, NaN after it.
 template <bool BF16>
@@ -774,7 +775,9 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
           acc = double(P.uniforms[t0 + w0 + lane]) * q < p;  // u < p / q
         }
         const uint32_t rej = __ballot_sync(kFull, lane < n && !acc);
-        L = rej ? w0 + __ffs(rej) - 1 : (w0 + n == k ? k : -1);  // -1: carry on
+        // every position accepted: L = k only if this wave also filtered the
+        // bonus row (a spare warp was left); otherwise the next wave does
+        L = rej ? w0 + __ffs(rej) - 1 : (w0 + n == k && 2 * n < kWarps ? k : -1);
         if (P.out_pq && lane < n && (L < 0 || w0 + lane <= L)) {
           P.out_pq[2 * int64_t(d0 + w0 + lane)] = p;
           P.out_pq[2 * int64_t(d0 + w0 + lane) + 1] = q;

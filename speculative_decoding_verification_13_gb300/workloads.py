@@ -145,17 +145,25 @@ def _sample_draft_tokens(draft, temps, top_k, top_p, owner, g, chunk):
         greedy = T == 0
         Ts = torch.where(greedy, torch.ones_like(T), T)
         z = x / Ts[:, None]
-        kk = int(tk.max().item()) if tk.numel() else 0
-        if 0 < kk < V and bool((tk > 0).all()):
+        on = (tk > 0) & (tk < V)
+        n_on = int(on.sum().item())
+        samp = None
+        if n_on < r1 - r0:  # rows without top-k: the whole softmax
+            samp = torch.multinomial(torch.softmax(z, dim=1), 1, generator=g).squeeze(1)
+        if n_on:
+            kk = int(torch.where(on, tk, torch.zeros_like(tk)).max().item())
             vals, idx = torch.topk(z, kk, dim=1)
-            pr = torch.softmax(vals, dim=1)
+            # each row's own top-k first (renormalised over it), then top-p
+            # (rows without top-k keep slot 0 here; their token comes from above)
+            col = torch.arange(kk, device=x.device)[None]
+            in_k = (col < tk[:, None]) & on[:, None] | (col == 0) & ~on[:, None]
+            pr = torch.softmax(vals.masked_fill(~in_k, float("-inf")), dim=1)
             before = torch.cumsum(pr, dim=1) - pr
-            keep = (before < tp[:, None]) & (torch.arange(kk, device=x.device)[None] < tk[:, None])
+            keep = (before < tp[:, None]) & in_k
             pr = torch.where(keep, pr, torch.zeros_like(pr))
             pick = torch.multinomial(pr, 1, generator=g).squeeze(1)
-            samp = idx.gather(1, pick[:, None]).squeeze(1)
-        else:
-            samp = torch.multinomial(torch.softmax(z, dim=1), 1, generator=g).squeeze(1)
+            samp_k = idx.gather(1, pick[:, None]).squeeze(1)
+            samp = samp_k if samp is None else torch.where(on, samp_k, samp)
         out[r0:r1] = torch.where(greedy, torch.argmax(x, dim=1), samp)
     return out.to(torch.int32)
 
