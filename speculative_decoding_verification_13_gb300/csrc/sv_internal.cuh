@@ -22,6 +22,7 @@ constexpr int kBufCap = 2560;                            // top-k candidate buff
 constexpr int kRegion = kBufCap / kConsumerWarps;        // per-warp region (fast path)
 constexpr int kRawCap = 1024;                            // top-k survivors kept per row
 constexpr int kScratch = 1024;                           // selection scratch entries
+constexpr int kStage = 64;                               // staged flagged vectors per warp
 constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
 constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
@@ -62,11 +63,24 @@ struct DrawDesc {
   int32_t t0, L;
 };
 
+// One entry of the row pass's work list, in request order (setup kernel).
+// The row pass reads the first six fields as 32-bit words, in this order.
+struct __align__(16) RowJob {
+  int32_t row;   // target rows 0 .. R_t - 1, then draft rows R_t ..
+  int32_t b;     // request
+  int32_t gx;    // token whose probability the row reports, or -1
+  int32_t mode;  // (position << 2) | row mode
+  float T;       // the request's temperature
+  int32_t K;     // the request's top-k (filtered rows)
+  int32_t pad[2];
+};
+static_assert(sizeof(RowJob) == 32, "row job layout");
+
 struct Ws {
   WsHeader* hdr;
   int32_t* t_off;    // [B + 1]
   int32_t* req_flag; // [B]
-  int4* rowlist;     // [R] {row, request, gather token, (pos << 2) | mode}
+  RowJob* rowlist;   // [R] rows the row pass streams
   RowStat* stats;    // [R]
   int32_t* cand_idx; // [R, kTopkMax]
   float* cand_p;     // [R, kTopkMax] kept probabilities
@@ -91,7 +105,7 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   size_t o = align256(sizeof(WsHeader));
   L.off_t_off = o;   o = align256(o + sizeof(int32_t) * (size_t)(B + 1));
   L.off_flag = o;    o = align256(o + sizeof(int32_t) * (size_t)(B > 0 ? B : 1));
-  L.off_rowlist = o; o = align256(o + sizeof(int4) * (size_t)(R > 0 ? R : 1));
+  L.off_rowlist = o; o = align256(o + sizeof(RowJob) * (size_t)(R > 0 ? R : 1));
   L.off_stats = o;   o = align256(o + sizeof(RowStat) * (size_t)(R > 0 ? R : 1));
   L.off_cidx = o;    o = align256(o + sizeof(int32_t) * kTopkMax * (size_t)(R > 0 ? R : 1));
   L.off_cp = o;      o = align256(o + sizeof(float) * kTopkMax * (size_t)(R > 0 ? R : 1));
@@ -111,7 +125,7 @@ inline Ws ws_bind(void* base, const WsLayout& L) {
   w.hdr = reinterpret_cast<WsHeader*>(p);
   w.t_off = reinterpret_cast<int32_t*>(p + L.off_t_off);
   w.req_flag = reinterpret_cast<int32_t*>(p + L.off_flag);
-  w.rowlist = reinterpret_cast<int4*>(p + L.off_rowlist);
+  w.rowlist = reinterpret_cast<RowJob*>(p + L.off_rowlist);
   w.stats = reinterpret_cast<RowStat*>(p + L.off_stats);
   w.cand_idx = reinterpret_cast<int32_t*>(p + L.off_cidx);
   w.cand_p = reinterpret_cast<float*>(p + L.off_cp);

@@ -14,8 +14,9 @@
 //   kArgmax - greedy: argmax of the raw logits, lowest index on ties.
 //   kTopk   - the top-k candidates of a filtered row: a speculative threshold
 //             from the first tile (the r-th largest per-vector maximum), then
-//             every tile's vectors are flagged against it and the candidates
-//             are appended to per-warp shared queues; the survivors (at least
+//             every tile's vectors are flagged against it, the flagged
+//             vectors are staged per warp and their elements at or above it
+//             become candidates; the survivors (at least
 //             k, at most kRawCap) are published unsorted for the filter
 //             kernel, which selects the exact top k.  A failed speculation is
 //             redone exactly from global memory (certified radix selection).
@@ -34,7 +35,10 @@ constexpr size_t kOffBuf = size_t(kStages) * kTileBytes;
 constexpr size_t kOffScratch = kOffBuf + size_t(kBufCap) * 8;
 constexpr size_t kOffXchg = kOffScratch + size_t(kScratch) * 8;
 constexpr size_t kOffBars = kOffXchg + size_t(2 * kConsumers) * 8;
-constexpr size_t kSmemBytes = kOffBars + size_t(2 * kStages) * 8;
+constexpr size_t kOffStage = kOffBars + size_t(2 * kStages) * 8;
+constexpr size_t kOffStageIdx = kOffStage + size_t(kConsumerWarps) * kStage * 16;
+constexpr size_t kSmemBytes = kOffStageIdx + size_t(kConsumerWarps) * kStage * 4;
+static_assert(kOffStage % 16 == 0, "staged vectors are 16-byte aligned");
 static_assert(kRowpassCtasPerSm * (kSmemBytes + 4096 + 1024) <= 228 * 1024,
               "shared memory budget for the resident CTAs of one SM");
 
@@ -50,9 +54,9 @@ struct RowShared {
   int cabort;
   int pabort;
   int bad;
+  unsigned int nbad;
   int kp;
   int wcnt[kConsumerWarps];
-  uint16_t queue[kConsumerWarps][(kTileBytes / 16 + kConsumers - 1) / kConsumers * 32];
   float v0;
   double wp;
   double inv_wp;
@@ -91,6 +95,11 @@ struct Elt<true> {
   __device__ static float scalar(const void* row, int64_t i) {
     return __uint_as_float(uint32_t(static_cast<const uint16_t*>(row)[i]) << 16);
   }
+  // Element e (0..7) of the vector.
+  __device__ static float elem(const uint4& q, int e) {
+    const uint32_t w = e < 4 ? (e < 2 ? q.x : q.y) : (e < 6 ? q.z : q.w);
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
 };
 
 template <>
@@ -108,6 +117,10 @@ struct Elt<false> {
   __device__ static float scalar(const void* row, int64_t i) {
     return static_cast<const float*>(row)[i];
   }
+  // Element e (0..3) of the vector.
+  __device__ static float elem(const uint4& q, int e) {
+    return __uint_as_float(e < 2 ? (e == 0 ? q.x : q.y) : (e == 2 ? q.z : q.w));
+  }
 };
 
 // Bounded wait with back-off: a waiting warp sleeps between polls so that it
@@ -122,21 +135,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
     __nanosleep(sleep_ns);
   }
   return false;
-}
-
-// Position of the n-th (0-based) set bit of x; x must hold more than n set bits.
-__device__ __forceinline__ int nth_set_bit(uint32_t x, int n) {
-  int pos = 0;
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1) {
-    const int c = __popc(x & ((1u << w) - 1u));
-    if (n >= c) {
-      n -= c;
-      x >>= w;
-      pos += w;
-    }
-  }
-  return pos;
 }
 
 // A bf16 value d below v (v itself a bf16 value), in both halves of a
@@ -204,6 +202,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     S.bnd[0] = S.bnd[1] = 0u;
     S.ins[0] = S.ins[1] = 0u;
     S.bad = 0;
+    S.nbad = 0u;
     S.thmin[0] = S.thmin[1] = ~0ull;
     S.tmpcount = 0;
   }
@@ -224,8 +223,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     long long issued = 0;
     bool stop = false;
     for (int j = blockIdx.x; j < n_active && !stop; j += gridDim.x) {
-      const int4 info = w.rowlist[j];
-      const int64_t row = info.x;
+      const int64_t row = w.rowlist[j].row;
       const char* src =
           row < P.Rt
               ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
@@ -284,21 +282,31 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       phase ^= 1u;
     }
   };
+  // vectors in tile t: full tiles, then the last (possibly partial) one
+  const int last_nvec = int((bulk - int64_t(ntiles - 1) * kTileBytes) / 16);
   auto tile_vectors = [&](int t) -> int {
-    const int64_t rem = bulk - int64_t(t) * kTileBytes;
-    return int((rem < kTileBytes ? rem : kTileBytes) / 16);
+    return t + 1 < ntiles ? kTileBytes / 16 : last_nvec;
   };
+  unsigned bad_seen = 0u;  // value of S.nbad after the previous row
 
+  // The next row's entry is loaded one row ahead, one 32-bit field per lane
+  // (lanes 0..5), and broadcast when its row starts.
+  auto load_entry = [&](int j) -> int {
+    return lane < 6 && j < n_active ? reinterpret_cast<const int*>(w.rowlist + j)[lane] : 0;
+  };
+  int nxt = load_entry(blockIdx.x);
   for (int j = blockIdx.x; j < n_active; j += gridDim.x) {
-    const int4 info = w.rowlist[j];
-    const int64_t row = info.x;
-    const int b = info.y;
-    const int gx = info.z;
-    const int mode = info.w & 3;
+    const int cur = nxt;
+    nxt = load_entry(j + gridDim.x);
+    const int64_t row = __shfl_sync(0xffffffffu, cur, 0);
+    const int b = __shfl_sync(0xffffffffu, cur, 1);
+    const int gx = __shfl_sync(0xffffffffu, cur, 2);
+    const int mode = __shfl_sync(0xffffffffu, cur, 3) & 3;
+    const float T = __int_as_float(__shfl_sync(0xffffffffu, cur, 4));
+    const int Kreq = __shfl_sync(0xffffffffu, cur, 5);
     const void* rowp =
         row < P.Rt ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
                    : static_cast<const char*>(P.draft) + (row - P.Rt) * P.d_stride * E::kSize;
-    const float T = P.temperature[b];
 
     if (mode == kStats) {
       // ---------------------------------------------- online softmax sums
@@ -465,8 +473,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       //
       // Thresholds: each warp takes the m-th largest of the keys it holds and
       // the CTA takes the minimum, so at least 8m keys reach it.
-      const int K = P.top_k[b];
-      const float tp = P.top_p ? P.top_p[b] : 1.0f;
+      const int K = Kreq;
       constexpr uint32_t kSkip = BF16 ? kSkipBf16 : kSkipF32;
       constexpr int VPT = (kTileBytes / 16 + kConsumers - 1) / kConsumers;
       constexpr int GROUP = 32 / EPV;
@@ -598,21 +605,75 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         }
         return ins;
       };
-      // Fast path: flag the tile's vectors with a packed max, then decode the
-      // flagged ones GROUP at a time (EPV lanes per vector) and append the
-      // passing elements to this warp's own buffer region.  No atomics and no
-      // barrier; a region overflow marks the row for the certified redo.
+      // Fast path: flag the tile's vectors with a packed max and copy the
+      // flagged ones (with their vector index in the row) to this warp's
+      // staging area; when it fills, and at the end of the row, one lane per
+      // staged vector tests its elements and the passing ones are appended to
+      // this warp's own buffer region.  Flagged vectors are few (about r per
+      // tile for the whole CTA), so the per-tile work stays a load, a packed
+      // compare and a vote.  No atomics and no barrier; a region overflow
+      // marks the row for the certified redo.
       uint64_t* region = buf + cwarp * kRegion;
+      uint4* stg_v = reinterpret_cast<uint4*>(smem + kOffStage) + cwarp * kStage;
+      int* stg_i = reinterpret_cast<int*>(smem + kOffStageIdx) + cwarp * kStage;
       int wcnt = 0;  // fill of this warp's region (warp-uniform)
-      auto fused_pass = [&](const uint4* tile, int nvec, int t, uint64_t th) {
+      int sn = 0;    // staged vectors of this warp (warp-uniform)
+      auto drain = [&](uint64_t th) {
         const float thv = composite_value(th);
         const uint32_t lt = (1u << lane) - 1u;
-        uint16_t* queue = S.queue[cwarp];
-        int qn = 0;  // flagged vectors of this warp in this tile (warp-uniform)
+        __syncwarp();
+        for (int b0 = 0; b0 < sn; b0 += 32) {
+          uint32_t mbits = 0u;
+          uint4 q = make_uint4(0u, 0u, 0u, 0u);
+          int vi = 0;
+          if (b0 + lane < sn) {
+            q = stg_v[b0 + lane];
+            vi = stg_i[b0 + lane];
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)  // also NaN and +inf (checked below)
+              if (!(E::elem(q, e) < thv)) mbits |= 1u << e;
+          }
+          while (__any_sync(0xffffffffu, mbits != 0u)) {
+            uint64_t key = 0ull;
+            bool pass = false;
+            if (mbits) {
+              const int e = __ffs(mbits) - 1;
+              mbits &= mbits - 1u;
+              const float xe = E::elem(q, e);
+              if (xe != xe || xe == INFINITY) {
+                bad = true;
+              } else {
+                key = composite_key(xe, uint32_t(vi * EPV + e));
+                pass = key >= th;
+              }
+            }
+            const uint32_t pm = __ballot_sync(0xffffffffu, pass);
+            if (pass) {
+              const int sidx = wcnt + __popc(pm & lt);
+              if (sidx < kRegion) region[sidx] = key;
+            }
+            wcnt += __popc(pm);
+          }
+        }
+        sn = 0;
+        __syncwarp();  // the staging area is rewritten next
+      };
+      // Stage the flagged vectors of one ballot (at most 32 of them).
+      auto stage = [&](bool c, const uint4& q, int vrow, uint32_t bal, uint64_t th) {
+        const int nf = __popc(bal);
+        if (sn + nf > kStage) drain(th);
+        if (c) {
+          const int slot = sn + __popc(bal & ((1u << lane) - 1u));
+          stg_v[slot] = q;
+          stg_i[slot] = vrow;
+        }
+        sn += nf;
+      };
+      auto fused_pass = [&](const uint4* tile, int nvec, int t, uint64_t th, float thv,
+                            [[maybe_unused]] uint32_t below2) {
+        const int vt = t * (kTileBytes / 16);  // first vector of the tile in the row
         if (nvec == kTileBytes / 16) {
           // full tile: two vectors per compare, no bounds checks
-          [[maybe_unused]] uint32_t below2 = 0u;
-          if constexpr (BF16) below2 = bf16_below2(thv);
 #pragma unroll
           for (int i = 0; i < VPT; i += 2) {
             const int va = ctid + i * kConsumers, vb = va + kConsumers;
@@ -630,50 +691,20 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
               cb = any && !(E::vmax(qb) < thv);
             }
             if (__any_sync(0xffffffffu, any)) {
-              const uint32_t ba = __ballot_sync(0xffffffffu, ca);
-              if (ca) queue[qn + __popc(ba & lt)] = uint16_t(va);
-              qn += __popc(ba);
-              const uint32_t bb = __ballot_sync(0xffffffffu, cb);
-              if (cb) queue[qn + __popc(bb & lt)] = uint16_t(vb);
-              qn += __popc(bb);
+              stage(ca, qa, vt + va, __ballot_sync(0xffffffffu, ca), th);
+              stage(cb, qb, vt + vb, __ballot_sync(0xffffffffu, cb), th);
             }
           }
         } else {
 #pragma unroll
           for (int i = 0; i < VPT; ++i) {
             const int v0 = ctid + i * kConsumers;
-            const bool c = v0 < nvec && !(E::vmax(tile[v0]) < thv);
-            const uint32_t bal = __ballot_sync(0xffffffffu, c);
-            if (c) queue[qn + __popc(bal & lt)] = uint16_t(v0);
-            qn += __popc(bal);
+            uint4 q = make_uint4(0u, 0u, 0u, 0u);
+            if (v0 < nvec) q = tile[v0];
+            const bool c = v0 < nvec && !(E::vmax(q) < thv);
+            stage(c, q, vt + v0, __ballot_sync(0xffffffffu, c), th);
           }
         }
-        if (qn == 0) return;
-        __syncwarp();
-        const int g = lane / EPV, e = lane % EPV;
-        const char* tb = reinterpret_cast<const char*>(tile);
-        for (int b0 = 0; b0 < qn; b0 += GROUP) {
-          const int n = b0 + g;
-          uint64_t key = 0ull;
-          bool pass = false;
-          if (n < qn) {
-            const int v = queue[n];
-            const float x = element(tb, v, e);
-            if (x != x || x == INFINITY) {
-              bad = true;
-            } else {
-              key = composite_key(x, uint32_t(t * kTileElems + v * EPV + e));
-              pass = key >= th;
-            }
-          }
-          const uint32_t pm = __ballot_sync(0xffffffffu, pass);
-          if (pass) {
-            const int sidx = wcnt + __popc(pm & lt);
-            if (sidx < kRegion) region[sidx] = key;
-          }
-          wcnt += __popc(pm);
-        }
-        __syncwarp();  // the queue is rewritten by the next tile
       };
       // Per-vector maximum in the composite order (value, first index).
       auto vector_max_key = [&](const uint4* tile, int v, int t) -> uint64_t {
@@ -873,13 +904,20 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         const float lam = float(K) * float(e0) / float(P.V);
         const int r = int(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f));
         const int L = (2 * r + kConsumerWarps - 1) / kConsumerWarps;
+        float thv = 0.0f;     // the threshold's value, and for bf16 the packed
+        uint32_t below2 = 0u; // flag pattern (fixed once tile 0 set theta)
         for (int t = 0; t < ntiles; ++t) {
           const uint4* tile = acquire();
           const int nvec = tile_vectors(t);
-          if (t == 0 && L <= 32 && nvec >= kConsumerWarps * L) bootstrap_spec(tile, nvec, 0, r, L);
-          fused_pass(tile, nvec, t, theta);
+          if (t == 0) {
+            if (L <= 32 && nvec >= kConsumerWarps * L) bootstrap_spec(tile, nvec, 0, r, L);
+            thv = composite_value(theta);
+            if constexpr (BF16) below2 = bf16_below2(thv);
+          }
+          fused_pass(tile, nvec, t, theta, thv, below2);
           release();
         }
+        drain(theta);
         // tail elements go to warp 0's region
         const bool tp_ok = ctid < n_tail;
         uint64_t tkey = 0ull;
@@ -903,8 +941,11 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         }
         if (lane == 0) S.wcnt[cwarp] = wcnt;
       }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad, 1);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicAdd(&S.nbad, 1u);
       consumer_sync();
+      // S.nbad only grows, so no reset (and no extra barrier) is needed
+      unsigned nb = *reinterpret_cast<volatile unsigned*>(&S.nbad);
+      bool rowbad = nb != bad_seen;
       {
         int tot = 0;
         bool ovf = false;
@@ -913,9 +954,9 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           ovf = ovf || S.wcnt[i] > kRegion;
         }
         count = tot;
-        redo = S.bad == 0 && (ovf || count < K);
+        redo = !rowbad && (ovf || count < K);
       }
-      if (!redo && S.bad == 0 && count > kRawCap) redo = true;  // too many survivors: exact path
+      if (!redo && !rowbad && count > kRawCap) redo = true;  // too many survivors: exact path
       if (redo) {
         // ---- certified path: the speculation missed; stream the row again
         consumer_sync();
@@ -934,13 +975,15 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           certified_tile(reinterpret_cast<const uint4*>(rowc + size_t(t) * kTileBytes),
                          tile_vectors(t), t);
         tail_insert();
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&S.bad, 1);
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicAdd(&S.nbad, 1u);
         consumer_sync();
+        nb = *reinterpret_cast<volatile unsigned*>(&S.nbad);
+        rowbad = nb != bad_seen;
         count = *reinterpret_cast<volatile int*>(&S.count);
         ins_seen[0] = *reinterpret_cast<volatile unsigned*>(&S.ins[0]);
         ins_seen[1] = *reinterpret_cast<volatile unsigned*>(&S.ins[1]);
         if (count > kBufCap) {  // only after a data error (the path above bounds the fill)
-          if (ctid == 0 && S.bad == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
+          if (ctid == 0 && !rowbad) flag_request(w, b, SV_ERR_INTERNAL, row);
           count = kBufCap;
         }
         if (count > K) compact(count);  // exact: the K largest in buf[0..K)
@@ -952,7 +995,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       // (certified path), contiguously; the finalize kernel selects the exact
       // top K from them and applies the temperature softmax and top-p.
       const size_t rbase = size_t(row) * kRawCap;
-      if (S.bad == 0) {
+      if (!rowbad) {
         if (redo) {
           for (int j = ctid; j < count; j += kConsumers) w.cand_raw[rbase + j] = buf[j];
         } else {
@@ -961,26 +1004,24 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           for (int j = lane; j < wcnt; j += 32) w.cand_raw[rbase + off + j] = region[j];
         }
       }
-      consumer_sync();
+      bad_seen = nb;
       if (ctid == 0) {
-        if (S.bad) flag_request(w, b, SV_ERR_DATA_LOGIT, row);
+        if (rowbad) flag_request(w, b, SV_ERR_DATA_LOGIT, row);
         RowStat st;
         st.s = 0.0;
         st.pg = __longlong_as_double(0x7ff8000000000000LL);
         st.m = 0.0f;
         st.arg = -1;
-        st.kept = S.bad ? 0 : count;
+        st.kept = rowbad ? 0 : count;
         st.mode = kTopk;
         w.stats[row] = st;
-        S.count = 0;
-        S.bad = 0;
-        S.ovf = 0;
-        S.tmpcount = 0;
       }
     }
 
-    // row boundary: a consistent view of the abort flag
-    consumer_sync();
+    // Row boundary.  S.cabort is written only inside acquire(), and every
+    // consumer thread has passed a barrier after its last acquire of this row
+    // (each mode ends with one) and none acquires again before the barrier
+    // below, so all threads read the same value here.
     const int ab = *reinterpret_cast<volatile int*>(&S.cabort);
     consumer_sync();
     if (ab) break;

@@ -143,14 +143,16 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     }
     if (b < P.B && active) {
       int a = a0;
+      const float T = P.temperature[b];
+      const int K = P.top_k ? P.top_k[b] : 0;
       for (int i = 0; i <= k; ++i) {
         const int gx = i < k ? P.draft_tokens[d0 + i] : -1;
-        w.rowlist[a++] = make_int4(t0 + i, b, gx, (i << 2) | mode_t);
+        w.rowlist[a++] = RowJob{t0 + i, b, gx, (i << 2) | mode_t, T, K, {0, 0}};
       }
       if (mode_d != kSkip)
         for (int i = 0; i < k; ++i)
-          w.rowlist[a++] =
-              make_int4((int)P.Rt + d0 + i, b, P.draft_tokens[d0 + i], (i << 2) | mode_d);
+          w.rowlist[a++] = RowJob{(int)P.Rt + d0 + i, b, P.draft_tokens[d0 + i],
+                                  (i << 2) | mode_d, T, K, {0, 0}};
     }
     if (b < P.B && (code || mode_d == kSkip)) {
       // Rows the streaming pass will not visit still get a defined record.
