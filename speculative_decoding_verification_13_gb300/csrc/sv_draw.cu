@@ -214,8 +214,10 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
         const uint32_t full = full0 + 8u * stage;
         mbar_arrive_expect_tx(full, dsrc ? 2u * bytes : bytes);
         unsigned char* dst = ring + size_t(stage) * kDStageBytes;
-        bulk_load(smem_addr(dst), tsrc + int64_t(s) * kDHalf, bytes, full);
-        if (dsrc) bulk_load(smem_addr(dst + kDHalf), dsrc + int64_t(s) * kDHalf, bytes, full);
+        const uint64_t pol = l2_evict_first_policy();
+        bulk_load_hint(smem_addr(dst), tsrc + int64_t(s) * kDHalf, bytes, full, pol);
+        if (dsrc)
+          bulk_load_hint(smem_addr(dst + kDHalf), dsrc + int64_t(s) * kDHalf, bytes, full, pol);
         ++issued;
         if (++stage == kDStages) {
           stage = 0;

@@ -1,28 +1,26 @@
 // Filter / decide kernel: what follows the row pass for every request except
 // the unfiltered sampled draws (the draw pass).
 //
-// Persistent warps over the job list of the setup kernel (one job per
-// filtered row, one decide job per other request):
-//   filtered row  (one warp) exact top k of the row pass's survivors
+// Persistent CTAs over the job lists of the setup kernel:
+//   filtered request  (one CTA) in waves of positions: a warp per target and
+//                 draft row takes the exact top k of the row pass's survivors
 //                 (composite order: logit descending, index ascending), the
 //                 temperature softmax over them, the top-p cut (keep j while
 //                 the mass before j is below top_p) and the renormalisation,
-//                 applied alike to target and draft rows ("Speculative decoding
-//                 and multi-token prediction", "Why the output is identical").
-//                 The warp that finishes a request's last row decides the
-//                 request and draws its final token from the kept sets.
-//   decide job    (one warp) greedy: accept while x_i equals the target argmax
-//                 (lowest index on ties) and emit the argmax at the first
-//                 disagreement or as the bonus ("DFlash" §4 step 5;
+//                 applied alike to target and draft rows ("Speculative
+//                 decoding and multi-token prediction", "Why the output is
+//                 identical"); one warp then accepts while u_i < p_i(x_i) /
+//                 q_i(x_i) ("FlashMap…" §4, steps 1-2) and, at the first
+//                 rejection or after the last draft, draws the final token
+//                 from the kept sets (§4 step 3).  Rows after the first
+//                 rejection are never filtered.
+//   decide job    (one warp per request) greedy: accept while x_i equals the
+//                 target argmax (lowest index on ties) and emit the argmax at
+//                 the first disagreement or as the bonus ("DFlash" §4 step 5;
 //                 "Speculative decoding…", "Draft and verify", step Three).
-//                 Sampling: accept while u_i < p_i(x_i) / q_i(x_i), stop at the
-//                 first rejection ("FlashMap…" §4, steps 1-2), then queue the
-//                 final draw for the draw pass.
-//
-// Completion counting ("the last one to finish does the rest"): a warp
-// publishes its row's results, fences, and bumps the request's counter; the
-// warp that sees the final count fences again and reads the other warps'
-// results through L2.  Nothing waits on another warp.
+//                 Unfiltered sampling: accept while u_i < p_i(x_i) / q_i(x_i),
+//                 stop at the first rejection, then queue the final draw for
+//                 the draw pass.
 #include <math.h>
 
 #include "sv_select.cuh"
@@ -222,26 +220,37 @@ __device__ __forceinline__ double scale2(double x, int n) {
 }
 
 // ------------------------------------------------------ filtered rows
-constexpr int kRegKeys = 16;  // survivors a lane holds (512 per warp); more go the slow way
+constexpr int kKeyCopy = 512;  // survivors copied to shared memory (more are read from L2)
+constexpr int kBinSort = 8;    // whole bins up to this size are ordered by insertion sort
+constexpr int kFastDraw = 64;  // kept sets up to this size are drawn from shared memory
+constexpr int kRankMax = 64;   // boundary bins up to this size are ordered by ranks
 
-// Per-warp scratch of one filtered row.
+// Per-warp scratch of one filtered row.  After the row it still holds the
+// row's kept set (sorted keys and probabilities) and p(x) of its token, which
+// the request's decision and final draw read.
+//
+// The per-row code runs once per row, so its instruction footprint, not its
+// arithmetic, sets its speed: the passes below are short loops over a
+// shared-memory copy of the survivors rather than unrolled register code.
 struct WarpSel {
-  uint64_t list[kTopkMax];  // the top k, unordered, then sorted descending
+  uint64_t keys[kKeyCopy];  // the row's survivors
+  uint64_t list[kTopkMax];  // the top k, sorted descending (composite order)
   union {
-    int hist[256];                        // survivors per value bin
+    uint64_t grp[kTopkMax];               // selection: keys of the boundary bin
     unsigned long long before[kTopkMax];  // fixed-point mass before j
   };
   union {
-    uint64_t grp[kTopkMax];   // during selection: the keys of the boundary bin
-    struct {                  // weights in sorted order, wf[j] * 2^we[j]
-      float wf[kTopkMax];
-      int we[kTopkMax];
+    struct {
+      float pk[kTopkMax];  // weight j as pk[j] * 2^hw[j]; then kept probability j
+      int hw[kTopkMax];    // selection: keys per value bin, then bin ends; weight exponents
     };
-    double wd[kTopkMax];      // weights in double (close top-p calls)
+    double wd[kTopkMax];   // weights in double (close top-p calls)
   };
-  int digit, above, cnt;
+  double pg;   // p(x) of the row's token, NaN without one
+  int kp;      // kept size
+  int fast;    // pk[0 .. kp) holds the kept probabilities and kp <= kFastDraw
+  int gcount;  // keys collected from the boundary bin
   int pad;
-  unsigned long long th;
 };
 
 union WarpScratch {
@@ -249,59 +258,24 @@ union WarpScratch {
   DrawScratch draw;
 };
 
-// A row's survivor keys for the selection passes: held in registers (lane
-// holds keys r * 32 + lane), or read from memory 512 at a time with every
-// lane's loads issued together.  each(f) calls f(key) on every slot, in step
-// across the warp (key 0 marks an empty slot).
-struct RegKeys {
-  const uint64_t (&key)[kRegKeys];
-  int nslot;  // slots past it hold no key (warp-uniform)
-  template <class F>
-  __device__ __forceinline__ void each(F f) const {
-#pragma unroll
-    for (int r = 0; r < kRegKeys; ++r) {
-      if (r >= nslot) break;
-      f(key[r]);
-    }
-  }
-};
-
-struct MemKeys {
-  const uint64_t* raw;
-  int n;
-  template <class F>
-  __device__ __forceinline__ void each(F f) const {
-    const int lane = threadIdx.x & 31;
-    for (int c0 = 0; c0 < n; c0 += 32 * kRegKeys) {
-      uint64_t key[kRegKeys];
-#pragma unroll
-      for (int r = 0; r < kRegKeys; ++r) {
-        const int e = c0 + r * 32 + lane;
-        key[r] = e < n ? __ldcg(raw + e) : 0ull;
-      }
-#pragma unroll
-      for (int r = 0; r < kRegKeys; ++r) f(key[r]);
-    }
-  }
-};
-
-// The K-th largest of n > K unique survivor keys, exactly.  One pass bins the
-// keys into 256 ordered bins, linear in the logit over [min, max] (a monotone
-// map); the bin holding the K-th largest is then resolved among its own keys.
-// Warp-uniform result.
-template <class Src>
-__device__ uint64_t select_kth(const Src& src, int K, WarpSel& ws, const uint64_t* raw, int n,
-                               uint32_t skip) {
+// The min(n, K) largest of the n unique survivor keys at keys[] (shared or
+// global memory), sorted descending into ws.list; returns their count.  One
+// pass bins the keys into 256 ordered bins linear in the logit over [min,
+// max] (a monotone map, so a higher bin holds only larger keys).  Bins wholly
+// inside the top K go straight to their final slots (a counting sort over
+// bins) and are then ordered within the bin; the bin holding the K-th largest
+// contributes its largest keys after them.
+__device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, WarpSel& ws,
+                                          const uint64_t* raw, uint32_t skip) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
   uint32_t lo = ~0u, hi = 0u;
-  src.each([&](uint64_t k) {
-    if (k) {
-      const uint32_t h = uint32_t(k >> 32);
-      lo = min(lo, h);
-      hi = max(hi, h);
-    }
-  });
+#pragma unroll 4
+  for (int e = lane; e < n; e += 32) {
+    const uint32_t h = uint32_t(keys[e] >> 32);
+    lo = min(lo, h);
+    hi = max(hi, h);
+  }
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
   // bins linear in the logit value (the order-preserving integer image is
@@ -316,17 +290,17 @@ __device__ uint64_t select_kth(const Src& src, int K, WarpSel& ws, const uint64_
     return min(255, int(x * scale));
   };
 #pragma unroll
-  for (int j = 0; j < 8; ++j) ws.hist[lane * 8 + j] = 0;
+  for (int j = 0; j < 8; ++j) ws.hw[lane * 8 + j] = 0;
+  if (lane == 0) ws.gcount = 0;
   __syncwarp();
-  src.each([&](uint64_t k) {
-    if (k) atomicAdd(&ws.hist[bin(k)], 1);
-  });
+#pragma unroll 4
+  for (int e = lane; e < n; e += 32) atomicAdd(&ws.hw[bin(keys[e])], 1);
   __syncwarp();
-  // the bin holding the K-th largest, the count above it and its own count
-  int cnt[8], loc = 0;
+  // lane holds bins 8 lane .. 8 lane + 7; off[j]: keys in the bins above
+  int cnt[8], off[8], loc = 0;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    cnt[j] = ws.hist[lane * 8 + j];
+    cnt[j] = ws.hw[lane * 8 + j];
     loc += cnt[j];
   }
   int suf = loc;
@@ -335,107 +309,142 @@ __device__ uint64_t select_kth(const Src& src, int K, WarpSel& ws, const uint64_
     const int y = __shfl_down_sync(kFull, suf, o);
     if (lane + o < 32) suf += y;
   }
-  int acc = suf - loc;
+  int acc = suf - loc, mine = -1;
+  bool big = false;  // a whole bin too large for insertion sort
 #pragma unroll
   for (int j = 7; j >= 0; --j) {
-    if (acc < K && acc + cnt[j] >= K) {
-      ws.digit = lane * 8 + j;
-      ws.above = acc;
-      ws.cnt = cnt[j];
-    }
+    off[j] = acc;
+    if (acc < K && acc + cnt[j] >= K) mine = j;  // the bin holding the K-th largest
     acc += cnt[j];
   }
-  __syncwarp();
-  const int bstar = ws.digit, need = K - ws.above, gcnt = ws.cnt;
-  if (gcnt == need) {
-    // the whole bin is kept: the threshold is its smallest key
-    uint64_t mn = ~0ull;
-    src.each([&](uint64_t k) {
-      if (k && bin(k) == bstar && k < mn) mn = k;
-    });
+  const uint32_t bm = __ballot_sync(kFull, mine >= 0);
+  int bstar = -1, above = n, gcnt = 0;  // n < K: every bin is kept whole
+  if (bm) {
+    const int bl = __ffs(bm) - 1;
+    int o = 0, c = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t y = shfl_xor_u64(mn, o);
-      mn = y < mn ? y : mn;
+    for (int j = 0; j < 8; ++j)
+      if (j == mine) {
+        o = off[j];
+        c = cnt[j];
+      }
+    bstar = bl * 8 + __shfl_sync(kFull, mine, bl);
+    above = __shfl_sync(kFull, o, bl);
+    gcnt = __shfl_sync(kFull, c, bl);
+  }
+  const int nsel = bm ? K : n;
+  const int P2 = max(32, next_pow2(nsel > 0 ? nsel : 1));
+  if (gcnt > kTopkMax) {
+    // a crowded boundary bin (many equal or nearly equal logits): the exact
+    // K-th largest by radix selection, then the keys reaching it, sorted
+    __syncwarp();
+    const uint64_t th = warp_select_kth(raw, n, K, ws.hw, &ws.kp, skip);
+    int c = 0;
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int e = e0 + lane;
+      const uint64_t k = e < n ? keys[e] : 0ull;
+      const bool keep = k != 0ull && k >= th;
+      const uint32_t bal = __ballot_sync(kFull, keep);
+      if (keep) {
+        const int sl = c + __popc(bal & lt);
+        if (sl < kTopkMax) ws.list[sl] = k;
+      }
+      c += __popc(bal);
     }
-    return mn;
+    for (int j = nsel + lane; j < P2; j += 32) ws.list[j] = 0ull;
+    __syncwarp();
+    sort_desc(ws.list, P2);
+    return nsel;
   }
-  if (gcnt > kTopkMax) return warp_select_kth(raw, n, K, ws.hist, &ws.digit, skip);
-  int g = 0;
-  src.each([&](uint64_t k) {
-    const bool in = k && bin(k) == bstar;
-    const uint32_t bal = __ballot_sync(kFull, in);
-    if (in) ws.grp[g + __popc(bal & lt)] = k;
-    g += __popc(bal);
-  });
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ws.hw[lane * 8 + j] = off[j];  // cursor: the bin's first slot
+    if (lane * 8 + j > bstar && cnt[j] > kBinSort) big = true;
+  }
+  big = __any_sync(kFull, big);
   __syncwarp();
-  if (gcnt <= 32) {
-    uint64_t v[1] = {lane < gcnt ? ws.grp[lane] : 0ull};
-    warp_sort_desc_regs<1>(v);
-    return __shfl_sync(kFull, static_cast<unsigned long long>(v[0]), need - 1);
-  }
-  // rank the bin's keys: the need-th largest is the threshold
-  for (int i = lane; i < gcnt; i += 32) {
-    const uint64_t ki = ws.grp[i];
-    int rk = 0;
-    for (int j = 0; j < gcnt; ++j) rk += ws.grp[j] > ki;
-    if (rk == need - 1) ws.th = ki;
+#pragma unroll 2
+  for (int e = lane; e < n; e += 32) {
+    const uint64_t k = keys[e];
+    const int bk = bin(k);
+    if (bk > bstar) ws.list[atomicAdd(&ws.hw[bk], 1)] = k;
+    else if (bk == bstar) ws.grp[atomicAdd(&ws.gcount, 1)] = k;
   }
   __syncwarp();
-  return ws.th;
+  if (bstar >= 0) {
+    // the boundary bin's largest K - above keys, in order: a key's rank among
+    // the bin's keys is its slot
+    const int need = K - above;
+    if (gcnt <= kRankMax) {
+      for (int e = lane; e < gcnt; e += 32) {
+        const uint64_t k = ws.grp[e];
+        int rk = 0;
+        for (int i = 0; i < gcnt; ++i) rk += ws.grp[i] > k;
+        if (rk < need) ws.list[above + rk] = k;
+      }
+    } else {
+      const int G = next_pow2(gcnt);
+      for (int j = gcnt + lane; j < G; j += 32) ws.grp[j] = 0ull;
+      __syncwarp();
+      sort_desc(ws.grp, G);
+      for (int j = lane; j < need; j += 32) ws.list[above + j] = ws.grp[j];
+    }
+  }
+  if (big) {
+    for (int j = nsel + lane; j < P2; j += 32) ws.list[j] = 0ull;
+    __syncwarp();
+    sort_desc(ws.list, P2);
+  } else {
+    // order inside each whole bin (bins above the boundary), by the lane that
+    // owns the bin; after the scatter hw[b] is the end of bin b, and bin b
+    // starts where bin b + 1 ends
+    for (int j = 0; j < 8; ++j) {
+      const int b = lane * 8 + j;
+      if (b <= bstar) continue;
+      const int o = b == 255 ? 0 : ws.hw[b + 1], e = ws.hw[b];
+      for (int a = o + 1; a < e; ++a) {
+        const uint64_t x = ws.list[a];
+        int c = a - 1;
+        while (c >= o && ws.list[c] < x) {
+          ws.list[c + 1] = ws.list[c];
+          --c;
+        }
+        ws.list[c + 1] = x;
+      }
+    }
+    __syncwarp();
+  }
+  return nsel;
 }
 
 // One filtered row, by one warp: the exact top k of the row pass's survivors
 // (composite order: logit descending, index ascending), the temperature
 // softmax over them, the top-p cut and the renormalisation; writes the kept
-// list, the kept size and p(x) of the row's draft token.  Weights are
-// float-accurate (relative error a few 1e-7) with exact fixed-point prefix
-// sums; a top-p cut within 2^-17 of the threshold is redone in double
-// precision, so the kept set is the double-precision one.
+// list, the kept size and p(x) of the row's draft token, and leaves the kept
+// set in ws.  Weights are float-accurate (relative error a few 1e-7) with
+// exact fixed-point prefix sums; a top-p cut within 2^-17 of the threshold is
+// redone in double precision, so the kept set is the double-precision one.
 template <bool BF16>
 __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float tp, int gx,
                                 WarpSel& ws) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
-  const uint32_t lt = (1u << lane) - 1u;
   const uint64_t* raw = w.cand_raw + size_t(row) * kRawCap;
-  // the first half of the key slots is fetched together with the survivor
-  // count (the row's kRawCap slots are all addressable)
-  uint64_t key[kRegKeys];
+  // the first 256 key slots are fetched together with the survivor count
+  // (the row's kRawCap slots are all addressable)
+  uint64_t pre[8];
 #pragma unroll
-  for (int r = 0; r < kRegKeys / 2; ++r) key[r] = __ldcg(raw + r * 32 + lane);
+  for (int r = 0; r < 8; ++r) pre[r] = __ldcg(raw + r * 32 + lane);
   const int n = min(max(w.stats[row].kept, 0), kRawCap);
-  const uint32_t skip = BF16 ? kSkipBf16 : kSkipF32;
-  int cnt = 0;
-  auto keep_top = [&](const auto& src, uint64_t th) {
-    src.each([&](uint64_t k) {
-      const bool keep = k && k >= th;
-      const uint32_t bal = __ballot_sync(kFull, keep);
-      if (keep) {
-        const int sl = cnt + __popc(bal & lt);
-        if (sl < kTopkMax) ws.list[sl] = k;
-      }
-      cnt += __popc(bal);
-    });
-  };
-  if (n <= 32 * kRegKeys) {
+  const int nc = min(n, kKeyCopy);
 #pragma unroll
-    for (int r = 0; r < kRegKeys; ++r) {
-      const int e = r * 32 + lane;
-      if (r >= kRegKeys / 2) key[r] = e < n ? __ldcg(raw + e) : 0ull;
-      else if (e >= n) key[r] = 0ull;  // keys are never 0
-    }
-    const RegKeys src{key, (n + 31) >> 5};
-    keep_top(src, n > K ? select_kth(src, K, ws, raw, n, skip) : 0ull);
-  } else {
-    const MemKeys src{raw, n};
-    keep_top(src, n > K ? select_kth(src, K, ws, raw, n, skip) : 0ull);
-  }
-  const int nsel = min(cnt, K);
-  const int Psz = max(32, next_pow2(nsel > 0 ? nsel : 1));
-  for (int j = nsel + lane; j < Psz; j += 32) ws.list[j] = 0ull;
+  for (int r = 0; r < 8; ++r)
+    if (r * 32 + lane < nc) ws.keys[r * 32 + lane] = pre[r];
+#pragma unroll 4
+  for (int e = 256 + lane; e < nc; e += 32) ws.keys[e] = __ldcg(raw + e);
   __syncwarp();
-  sort_desc(ws.list, Psz);
+  const int nsel = select_sorted(n <= kKeyCopy ? ws.keys : raw, n, K, ws, raw,
+                                 BF16 ? kSkipBf16 : kSkipF32);
 
   const float v0 = composite_value(ws.list[0]);
   // log2(e) / T split into two floats, formed once per row (the FP64 pipe is
@@ -462,8 +471,8 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
         f = weight_split(v, v0, chi, clo, &e2);
         fx = fix55(f, e2);
       }
-      ws.wf[j] = f;
-      ws.we[j] = e2;
+      ws.pk[j] = f;
+      ws.hw[j] = e2;
     }
     const unsigned long long incl = warp_incl_scan(fx);
     if (j < nsel) ws.before[j] = W + incl - fx;
@@ -519,6 +528,7 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   invd = __shfl_sync(kFull, invd, 0);
   const float invf = float(invd);
   const size_t cbase = size_t(row) * kTopkMax;
+  const bool fast = !exact && kp <= kFastDraw;
   float pgv = 0.f;
   bool hit = false;
   for (int j = lane; j < kp; j += 32) {
@@ -526,12 +536,13 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
     float pj;
     if (exact)
       pj = float(ws.wd[j] * invd);
-    else if (ws.we[j] > -100)
-      pj = ws.wf[j] * invf * __int_as_float((ws.we[j] + 127) << 23);
+    else if (ws.hw[j] > -100)
+      pj = ws.pk[j] * invf * __int_as_float((ws.hw[j] + 127) << 23);
     else
-      pj = float(scale2(double(ws.wf[j]), ws.we[j]) * invd);  // far below 2^-100: in double
+      pj = float(scale2(double(ws.pk[j]), ws.hw[j]) * invd);  // far below 2^-100: in double
     w.cand_idx[cbase + j] = idx;
     w.cand_p[cbase + j] = pj;
+    if (fast) ws.pk[j] = pj;  // same slot, same lane
     if (idx == gx) {
       hit = true;
       pgv = pj;
@@ -540,9 +551,13 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   const uint32_t hb = __ballot_sync(kFull, hit);
   if (hb) pgv = __shfl_sync(kFull, pgv, __ffs(hb) - 1);
   if (lane == 0) {
+    const double pg = gx >= 0 ? double(pgv) : nan64();
+    ws.pg = pg;
+    ws.kp = kp;
+    ws.fast = fast;
     RowStat st;
     st.s = Wp;
-    st.pg = gx >= 0 ? pgv : nan64();
+    st.pg = pg;
     st.m = v0;
     st.arg = -1;
     st.kept = kp;
@@ -730,32 +745,118 @@ __device__ __noinline__ int draw_kept(const Problem& P, int64_t tr, int64_t dr, 
   return -1;  // not reached: the second attempt always returns
 }
 
-constexpr int kPostThreads = 512;
+constexpr int kPostThreads = 256;
 constexpr int kWarps = kPostThreads / 32;
 constexpr int kWave = kWarps / 2;  // positions per wave: a target and a draft row each
 
 struct PostShared {
   int L;
+  int idx[kFastDraw];                // draw_fast: target kept tokens
+  unsigned long long r[kFastDraw];   // and their residual (or p) mass
 };
+
+// A float probability in [0, 1] as a multiple of 2^-55 (exact above 2^-31;
+// subnormals count as 0).
+__device__ __forceinline__ unsigned long long fix_prob(float p) {
+  return p >= 1.17549435e-38f ? fix55(p, 0) : 0ull;
+}
+
+// Final draw of a filtered request from kept sets held in shared memory (at
+// most kFastDraw tokens each), by inverse CDF in vocabulary-index order:
+// y = min{ y : C_y > u S } over the residual max(0, p - q) of the target's
+// kept tokens after a rejection (q = 0 outside the draft's kept set; p itself
+// when the residual mass is zero), or over p for the bonus draw.  Masses are
+// summed exactly in fixed point (multiples of 2^-55), so the order of the
+// additions does not matter; C_y is each token's own prefix, summed directly
+// rather than after an index sort.  One warp; warp-uniform result.
+__device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double u, PostShared& sh) {
+  const int lane = threadIdx.x & 31;
+  const int Kt = t.kp, Kd = d ? d->kp : 0;
+  int idx[2];
+  float p[2], q[2] = {0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int j = s * 32 + lane;
+    idx[s] = j < Kt ? composite_index(t.list[j]) : INT_MAX;
+    p[s] = j < Kt ? t.pk[j] : 0.f;
+  }
+  for (int i = 0; i < Kd; ++i) {
+    const int di = composite_index(d->list[i]);
+    const float dq = d->pk[i];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      if (di == idx[s]) q[s] = dq;
+  }
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    const bool residual = d != nullptr && attempt == 0;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int j = s * 32 + lane;
+      const unsigned long long fp = fix_prob(p[s]), fq = residual ? fix_prob(q[s]) : 0ull;
+      if (j < Kt) {
+        sh.idx[j] = idx[s];
+        sh.r[j] = fp > fq ? fp - fq : 0ull;
+      }
+    }
+    __syncwarp();
+    unsigned long long C[2] = {0ull, 0ull}, rmine[2] = {0ull, 0ull};
+    for (int i = 0; i < Kt; ++i) {
+      const int ii = sh.idx[i];
+      const unsigned long long ri = sh.r[i];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        if (ii <= idx[s]) C[s] += ri;
+        if (ii == idx[s]) rmine[s] = ri;
+      }
+    }
+    // S: the prefix of the largest kept index
+    unsigned long long S = max(C[0], C[1]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long y = shfl_xor_u64(S, o);
+      S = y > S ? y : S;
+    }
+    __syncwarp();  // sh is rewritten by a second attempt
+    if (S == 0ull && attempt == 0) continue;  // residual mass vanished: draw from p
+    unsigned long long th = 0ull;
+    if (lane == 0) th = static_cast<unsigned long long>(u * double(S));  // floor(u S)
+    th = __shfl_sync(kFull, th, 0);
+    int y = INT_MAX, last = -1;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      if (idx[s] != INT_MAX && C[s] > th) y = min(y, idx[s]);
+      if (rmine[s] > 0ull) last = max(last, idx[s]);
+    }
+    y = __reduce_min_sync(kFull, y);
+    last = __reduce_max_sync(kFull, last);
+    return y != INT_MAX ? y : last;  // rounding left no C above u S: the last token with mass
+  }
+  return -1;  // not reached: the second attempt always returns
+}
 
 // A filtered request, by one CTA, in waves of kWave positions: warps 2j and
 // 2j + 1 filter the target and draft rows of position w0 + j, the first spare
 // warp of the wave that reaches position k - 1 filters the bonus row k (when
 // that wave fills every warp, k a multiple of kWave, warp 0 of one more wave
-// does), then warp 0 decides the wave's positions in order.  Verification stops at the
-// first rejection, so rows past it are never filtered.  (p, q) are reported
-// for the positions up to the stop, NaN after it.
+// does), then warp 0 decides the wave's positions in order from the p(x), q(x)
+// the filtering warps left in shared memory.  Verification stops at the first
+// rejection, so rows past it are never filtered.  (p, q) are reported for the
+// positions up to the stop, NaN after it.  The final draw reads the kept sets
+// of the stopping position from the same shared memory (or, for kept sets
+// larger than kFastDraw, from the lists in global memory).
 template <bool BF16>
 __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScratch* scr,
                                  PostShared& sh) {
-  const Ws& w = P.ws;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int d0 = t0 - b;
   const int K = P.top_k[b];
   const float T = P.temperature[b];
   const float tp = P.top_p ? P.top_p[b] : 1.0f;
-  for (int w0 = 0;; w0 += kWave) {
+  int w0 = 0;
+  for (;; w0 += kWave) {
     const int pos = w0 + (warp >> 1);
+    float u = 0.f;  // warp 0: the uniform of position w0 + lane
+    if (warp == 0 && lane < kWave && w0 + lane < k) u = P.uniforms[t0 + w0 + lane];
     if (pos < k) {
       const int64_t row = (warp & 1) ? P.Rt + d0 + pos : int64_t(t0) + pos;
       warp_filter_row<BF16>(P, row, K, T, tp, P.draft_tokens[d0 + pos], scr[warp].sel);
@@ -770,9 +871,9 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
         bool acc = true;
         double p = 0.0, q = 0.0;
         if (lane < n) {
-          p = w.stats[t0 + w0 + lane].pg;
-          q = w.stats[P.Rt + d0 + w0 + lane].pg;
-          acc = double(P.uniforms[t0 + w0 + lane]) * q < p;  // u < p / q
+          p = scr[2 * lane].sel.pg;
+          q = scr[2 * lane + 1].sel.pg;
+          acc = double(u) * q < p;  // u < p / q
         }
         const uint32_t rej = __ballot_sync(kFull, lane < n && !acc);
         // every position accepted: L = k only if this wave also filtered the
@@ -790,8 +891,17 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
   }
   const int L = sh.L;
   if (warp == 0) {
-    const int y = draw_kept(P, t0 + L, P.Rt + d0 + L, L < k, double(P.uniforms[t0 + k]),
-                            scr[0].draw);
+    // the stopping position lies in the last wave: its target (or bonus) row
+    // was filtered by warp 2 (L - w0), its draft row by the next warp
+    const int tw = 2 * (L - w0);
+    const bool residual = L < k;
+    const double u = double(P.uniforms[t0 + k]);
+    const WarpSel& ts = scr[tw].sel;
+    int y;
+    if (ts.fast && (!residual || scr[tw + 1].sel.fast))
+      y = draw_fast(ts, residual ? &scr[tw + 1].sel : nullptr, u, sh);
+    else
+      y = draw_kept(P, t0 + L, P.Rt + d0 + L, residual, u, scr[0].draw);
     for (int i = lane; i <= k; i += 32)
       P.out_tokens[t0 + i] = i < L ? P.draft_tokens[d0 + i] : (i == L ? y : -1);
     if (P.out_pq)

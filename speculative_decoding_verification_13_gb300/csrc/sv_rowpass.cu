@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     if (lane != 0) return;
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
+    const uint64_t stream_pol = l2_evict_first_policy();
     bool stop = false;
     for (int j = blockIdx.x; j < n_active && !stop; j += gridDim.x) {
       const int64_t row = w.rowlist[j].row;
@@ -238,8 +239,8 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           break;
         }
         mbar_arrive_expect_tx(full0 + 8u * stage, bytes);
-        bulk_load(smem_addr(ring + size_t(stage) * kTileBytes), src + int64_t(t) * kTileBytes,
-                  bytes, full0 + 8u * stage);
+        bulk_load_hint(smem_addr(ring + size_t(stage) * kTileBytes), src + int64_t(t) * kTileBytes,
+                       bytes, full0 + 8u * stage, stream_pol);
         ++issued;
         if (++stage == kStages) {
           stage = 0;

@@ -10,32 +10,37 @@ namespace {
 
 constexpr int kSetupThreads = 1024;
 
-// Exclusive scan over the CTA; *total receives the sum.
-__device__ int block_exclusive_scan(int v, int* total) {
-  __shared__ int s_warp[kSetupThreads / 32];
+// Exclusive scan over the CTA; *total receives the sum.  Two counters travel
+// packed in one 64-bit word (each field's sum over a chunk stays below 2^32).
+__device__ unsigned long long block_exclusive_scan(unsigned long long v, unsigned long long* total) {
+  __shared__ unsigned long long s_warp[kSetupThreads / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  unsigned long long x = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
   if (lane == 31) s_warp[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int y = s_warp[lane];
+    unsigned long long y = s_warp[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int z = __shfl_up_sync(0xffffffffu, y, o);
+      const unsigned long long z = __shfl_up_sync(0xffffffffu, y, o);
       if (lane >= o) y += z;
     }
     s_warp[lane] = y;
   }
   __syncthreads();
-  const int excl = x - v + (warp ? s_warp[warp - 1] : 0);
+  const unsigned long long excl = x - v + (warp ? s_warp[warp - 1] : 0ull);
   *total = s_warp[kSetupThreads / 32 - 1];
   __syncthreads();
   return excl;
+}
+
+__device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
+  return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
@@ -55,24 +60,36 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   __syncthreads();
 
   // Pass 1: row offsets; a k outside [0, SV_MAX_K] makes the layout undefined.
+  // With a single chunk (B <= kSetupThreads) every per-request value read or
+  // formed here stays in registers for pass 2.
+  const bool one = P.B <= kSetupThreads;
+  int k1 = 0, t01 = 0, tk1 = 0;
+  float T1 = 0.f, tp1 = 1.0f;
   int carry = 0, carry_d = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int k = 0;
     if (b < P.B) {
       k = P.k_per_req[b];
+      if (one) {
+        T1 = P.temperature[b];
+        tp1 = P.top_p ? P.top_p[b] : 1.0f;
+        tk1 = P.top_k ? P.top_k[b] : 0;
+      }
       if (k < 0 || k > SV_MAX_K) {
         record_error(w.hdr, SV_ERR_DATA_K, b, -1);
         atomicOr(&s_bad, 1);
         k = 0;
       }
     }
-    int tot, totd;
-    const int ex = block_exclusive_scan(b < P.B ? k + 1 : 0, &tot);
-    block_exclusive_scan(b < P.B ? k : 0, &totd);
-    if (b < P.B) w.t_off[b] = carry + ex;
-    carry += tot;
-    carry_d += totd;
+    unsigned long long tot;
+    const unsigned long long ex =
+        block_exclusive_scan(b < P.B ? pack2(uint32_t(k + 1), uint32_t(k)) : 0ull, &tot);
+    if (b < P.B) w.t_off[b] = carry + int(uint32_t(ex));
+    k1 = k;
+    t01 = carry + int(uint32_t(ex));
+    carry += int(uint32_t(tot));
+    carry_d += int(uint32_t(tot >> 32));
   }
   if (threadIdx.x == 0) {
     w.t_off[P.B] = carry;
@@ -91,13 +108,15 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int code = 0, active = 0, mode_t = kSkip, mode_d = kSkip, k = 0, t0 = 0, d0 = 0;
+    float T = 0.f;
+    int tk = 0;
     if (b < P.B) {
-      k = P.k_per_req[b];
-      t0 = w.t_off[b];
+      k = one ? k1 : P.k_per_req[b];
+      t0 = one ? t01 : w.t_off[b];
       d0 = t0 - b;
-      const float T = P.temperature[b];
-      const float tp = P.top_p ? P.top_p[b] : 1.0f;
-      const int tk = P.top_k ? P.top_k[b] : 0;
+      T = one ? T1 : P.temperature[b];
+      const float tp = one ? tp1 : (P.top_p ? P.top_p[b] : 1.0f);
+      tk = one ? tk1 : (P.top_k ? P.top_k[b] : 0);
       const bool topk_on = tk > 0 && tk < P.V;
       const bool filtered = T > 0.0f && (topk_on || tp < 1.0f);
       if (!(T >= 0.0f) || isinf(T)) code = SV_ERR_DATA_TEMPERATURE;
@@ -127,13 +146,17 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       }
     }
     const bool filt = !code && mode_t == kTopk;
-    int tot, totf, toto;
-    const int a0 = carry_a + block_exclusive_scan(active, &tot);
-    carry_a += tot;
-    const int f0 = carry_f + block_exclusive_scan(b < P.B && filt ? 1 : 0, &totf);
-    carry_f += totf;
-    const int o0 = carry_o + block_exclusive_scan(b < P.B && !filt ? 1 : 0, &toto);
-    carry_o += toto;
+    // active rows (low half); filtered requests and the others (high half,
+    // 16 bits each: a chunk holds at most kSetupThreads requests)
+    unsigned long long tot;
+    const uint32_t fo = b < P.B ? (filt ? 1u : 1u << 16) : 0u;
+    const unsigned long long ex = block_exclusive_scan(pack2(uint32_t(active), fo), &tot);
+    const int a0 = carry_a + int(uint32_t(ex));
+    const int f0 = carry_f + int((ex >> 32) & 0xffffu);
+    const int o0 = carry_o + int(ex >> 48);
+    carry_a += int(uint32_t(tot));
+    carry_f += int((tot >> 32) & 0xffffu);
+    carry_o += int(tot >> 48);
     if (b < P.B) {
       w.seg_cnt[b] = 0;
       if (filt)
@@ -143,16 +166,14 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     }
     if (b < P.B && active) {
       int a = a0;
-      const float T = P.temperature[b];
-      const int K = P.top_k ? P.top_k[b] : 0;
       for (int i = 0; i <= k; ++i) {
         const int gx = i < k ? P.draft_tokens[d0 + i] : -1;
-        w.rowlist[a++] = RowJob{t0 + i, b, gx, (i << 2) | mode_t, T, K, {0, 0}};
+        w.rowlist[a++] = RowJob{t0 + i, b, gx, (i << 2) | mode_t, T, tk, {0, 0}};
       }
       if (mode_d != kSkip)
         for (int i = 0; i < k; ++i)
           w.rowlist[a++] = RowJob{(int)P.Rt + d0 + i, b, P.draft_tokens[d0 + i],
-                                  (i << 2) | mode_d, T, K, {0, 0}};
+                                  (i << 2) | mode_d, T, tk, {0, 0}};
     }
     if (b < P.B && (code || mode_d == kSkip)) {
       // Rows the streaming pass will not visit still get a defined record.
