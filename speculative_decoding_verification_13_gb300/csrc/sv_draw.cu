@@ -167,6 +167,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     S.pabort = 0;
   }
   __syncthreads();
+  pdl_wait();  // the filter / decide kernel's queue
   const int n_draw = w.hdr->n_draw;
   const int V = P.V;
   const int ntile = (V + kDTile - 1) / kDTile;
@@ -471,10 +472,8 @@ size_t draw_pass_smem_bytes(int V) {
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s) {
   const size_t smem = draw_pass_smem_bytes(P.V);
   if (bf16)
-    draw_pass_kernel<true><<<grid, kDThreads, smem, s>>>(P);
-  else
-    draw_pass_kernel<false><<<grid, kDThreads, smem, s>>>(P);
-  return cudaGetLastError();
+    return launch_after(draw_pass_kernel<true>, grid, kDThreads, smem, s, P);
+  return launch_after(draw_pass_kernel<false>, grid, kDThreads, smem, s, P);
 }
 
 // Shared-memory limit (largest vocabulary) and resident CTAs per SM for a

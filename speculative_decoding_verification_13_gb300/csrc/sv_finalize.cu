@@ -922,6 +922,8 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
   __shared__ PostShared sh;
   const Ws& w = P.ws;
   const int warp = threadIdx.x >> 5;
+  pdl_wait();     // the row pass's results
+  pdl_trigger();  // the draw pass may launch; it waits for this kernel
   if (w.hdr->global_err) {
     // batch-level data error: every output is -1 (NaN for the probabilities)
     const int64_t stride = int64_t(gridDim.x) * kPostThreads;
@@ -957,10 +959,8 @@ size_t filter_smem_bytes() { return sizeof(WarpScratch) * kWarps; }
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s) {
   const size_t smem = filter_smem_bytes();
   if (bf16)
-    filter_decide_kernel<true><<<grid, kPostThreads, smem, s>>>(P);
-  else
-    filter_decide_kernel<false><<<grid, kPostThreads, smem, s>>>(P);
-  return cudaGetLastError();
+    return launch_after(filter_decide_kernel<true>, grid, kPostThreads, smem, s, P);
+  return launch_after(filter_decide_kernel<false>, grid, kPostThreads, smem, s, P);
 }
 
 // Shared-memory limit and resident CTAs per SM of the filter / decide kernel

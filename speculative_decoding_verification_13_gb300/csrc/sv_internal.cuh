@@ -165,6 +165,25 @@ cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStre
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 size_t rowpass_smem_bytes();
 
+// Launch of a kernel that may start while the previous kernel on the stream
+// finishes (programmatic dependent launch): it must execute pdl_wait() before
+// touching memory that the previous kernel writes or reads.
+template <class Kern>
+inline cudaError_t launch_after(Kern kernel, int grid, int threads, size_t smem, cudaStream_t s,
+                                const Problem& P) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(unsigned(threads));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
 // ------------------------------------------------------------ device helpers
 #ifdef __CUDACC__
 
@@ -253,6 +272,14 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, ui
       "[%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// Programmatic dependent launch: wait until the previous kernel on the stream
+// has completed and its writes are visible (a no-op when the kernel was
+// launched normally); let the next kernel on the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Barrier among the consumer warps only (the producer warp never joins).

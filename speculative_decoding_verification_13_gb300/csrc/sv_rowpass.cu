@@ -207,6 +207,8 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     S.tmpcount = 0;
   }
   __syncthreads();
+  pdl_wait();     // the setup kernel's lists and header
+  pdl_trigger();  // the filter kernel may launch; it waits for this kernel
 
   const int n_active = w.hdr->n_active;
   const int64_t row_bytes = int64_t(P.V) * E::kSize;
@@ -1035,10 +1037,8 @@ size_t rowpass_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s) {
   if (bf16)
-    rowpass_kernel<true><<<grid, kRowpassThreads, kSmemBytes, s>>>(P);
-  else
-    rowpass_kernel<false><<<grid, kRowpassThreads, kSmemBytes, s>>>(P);
-  return cudaGetLastError();
+    return launch_after(rowpass_kernel<true>, grid, kRowpassThreads, kSmemBytes, s, P);
+  return launch_after(rowpass_kernel<false>, grid, kRowpassThreads, kSmemBytes, s, P);
 }
 
 cudaError_t rowpass_configure() {

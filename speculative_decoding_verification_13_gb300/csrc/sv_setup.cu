@@ -46,6 +46,7 @@ __device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   const Ws& w = P.ws;
   __shared__ int s_bad;
+  pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
   if (threadIdx.x == 0) {
     w.hdr->err_code = 0;
     w.hdr->err_req = -1;
