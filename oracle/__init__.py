@@ -1,4 +1,5 @@
-"""Oracle for batched speculative-decoding verification.
+"""Oracle for batched speculative-decoding verification and for the draft-side
+sampler that produces the tokens it verifies.
 
 TEST INFRASTRUCTURE ONLY.  ``oracle.cpp`` states, in plain single-threaded
 double-precision C++, what verification computes (the rejection rule of
@@ -63,6 +64,8 @@ def load_variant(path: str):
     lib.oracle_row_probs.argtypes = [i32, i32, P, f32, i32, f32, P, P]
     lib.oracle_argmax.restype = i32
     lib.oracle_argmax.argtypes = [i32, i32, P]
+    lib.oracle_draft_sample.restype = i32
+    lib.oracle_draft_sample.argtypes = [i32, i32, i32, P, i64, i64, P, P, P, P, P, P, P, P]
     return lib
 
 
@@ -214,6 +217,45 @@ def row_probs(row, temperature, top_k=0, top_p=1.0):
     if rc != 0:
         raise ValueError(f"oracle_row_probs failed with code {rc}")
     return p, float(m[0])
+
+
+def draft_sample(logits, k_per_req, temperature, uniforms, top_k=None, top_p=None,
+                 threads: int = 1):
+    """Draft-side sampling over drafter rows laid out like the verifier's draft
+    rows (request b owns rows d_off[b]..d_off[b]+k_b-1).  Returns a dict with
+    ``tokens`` [R] int32 (-1 for failed requests), ``q`` [R] float64
+    (q_i(x_i), NaN for greedy / failed rows) and ``margins`` [R, 2]
+    (m_cdf, m_topp).  ``threads > 1`` evaluates groups of requests
+    concurrently with the same code."""
+    xl, dt = as_logits(logits)
+    k = _np(k_per_req, np.int32)
+    B = int(k.shape[0])
+    T = _np(temperature, np.float32)
+    tk = _np(top_k, np.int32) if top_k is not None else np.zeros(B, np.int32)
+    tp = _np(top_p, np.float32) if top_p is not None else np.ones(B, np.float32)
+    u = _np(uniforms, np.float32)
+    R, V = int(xl.shape[0]), int(xl.shape[1])
+    tok = np.full(max(R, 1), -1, np.int32)
+    q = np.full(max(R, 1), np.nan)
+    mg = np.full((max(R, 1), 2), np.nan)
+    lib = _lib()
+    d_off = np.concatenate([[0], np.cumsum(k.astype(np.int64))])
+
+    def run(lo, hi):
+        r0, r1 = int(d_off[lo]), int(d_off[hi])
+        return lib.oracle_draft_sample(hi - lo, V, dt, _ptr(xl[r0:r1]), r1 - r0, V,
+                                       _ptr(k[lo:hi]), _ptr(T[lo:hi]), _ptr(tk[lo:hi]),
+                                       _ptr(tp[lo:hi]), _ptr(u[r0:r1]), _ptr(tok[r0:r1]),
+                                       _ptr(q[r0:r1]), _ptr(mg[r0:r1]))
+
+    if d_off[-1] != R or threads <= 1 or B <= 1 or (k < 0).any() or (k > 32).any():
+        rc = lib.oracle_draft_sample(B, V, dt, _ptr(xl), R, V, _ptr(k), _ptr(T), _ptr(tk),
+                                     _ptr(tp), _ptr(u), _ptr(tok), _ptr(q), _ptr(mg))
+    else:
+        bounds = np.linspace(0, B, min(threads, B) + 1).astype(int)
+        with ThreadPoolExecutor(len(bounds) - 1) as ex:
+            rc = max(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+    return dict(rc=rc, tokens=tok[:R], q=q[:R], margins=mg[:R])
 
 
 def argmax(row) -> int:

@@ -1,4 +1,5 @@
-// Speculative-decoding verification oracle.
+// Speculative-decoding verification oracle (and the draft-side sampler that
+// produces the drafted tokens it verifies).
 //
 // TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
 // statement of what batched speculative-decoding verification computes.  It is
@@ -470,6 +471,93 @@ int oracle_row_probs(int32_t vocab, int32_t dtype, const void* row, float temper
   }
   std::copy(p.begin(), p.end(), out_p);
   if (out_topp_margin) *out_topp_margin = m;
+  return OR_OK;
+}
+
+// Draft-side sampling ([FM] §5 draft_block step 5: logits / temperature,
+// softmax, a multinomial draw; argmax at temperature 0), for a batch laid out
+// like the verifier's draft rows: request b owns rows d_off[b] .. d_off[b] +
+// k_b - 1 with d_off[b] = sum_{j<b} k_j.  Row i of request b draws
+//   x_i = min{ y : C_y > u_i * S }  (reading R3; S = sum of the row's p)
+// from the row's distribution at the request's temperature with its top-k /
+// top-p filter (R4, R7), or takes the argmax of the raw logits, lowest index on
+// ties, at temperature 0 (R8).  u_i = uniforms[d_off[b] + i].
+//   out_tokens [rows]: x_i, -1 for every row of a request with a data error
+//   out_q      [rows] (may be NULL): q_i(x_i), NaN for greedy and failed rows
+//   out_margins [rows, 2] (may be NULL): (m_cdf, m_topp) of the row, +inf
+//              where no such decision was taken, NaN for failed rows
+// Returns 0, or a batch-level error (the row count does not match sum k_b;
+// every token is then -1).
+int oracle_draft_sample(int32_t batch, int32_t vocab, int32_t dtype, const void* logits,
+                        int64_t rows, int64_t stride, const int32_t* k_per_req,
+                        const float* temperature, const int32_t* top_k, const float* top_p,
+                        const float* uniforms, int32_t* out_tokens, double* out_q,
+                        double* out_margins) {
+  if (batch < 0 || vocab < 1 || (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F64) ||
+      (rows > 0 && !logits) || !k_per_req || !temperature || (rows > 0 && !uniforms) ||
+      (rows > 0 && !out_tokens))
+    return OR_ERR_ARG;
+  int64_t total = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (k_per_req[b] < 0 || k_per_req[b] > kMaxK) {
+      total = -1;
+      break;
+    }
+    total += k_per_req[b];
+  }
+  const double nan = std::nan("");
+  auto fail_rows = [&](int64_t r0, int64_t n) {
+    for (int64_t r = r0; r < r0 + n; ++r) {
+      out_tokens[r] = -1;
+      if (out_q) out_q[r] = nan;
+      if (out_margins) out_margins[2 * r] = out_margins[2 * r + 1] = nan;
+    }
+  };
+  if (total != rows) {
+    fail_rows(0, rows);
+    return OR_ERR_ROWS;
+  }
+  int64_t d0 = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int k = k_per_req[b];
+    const float T = temperature[b];
+    const int tk = top_k ? top_k[b] : 0;
+    const float tp = top_p ? top_p[b] : 1.0f;
+    bool ok = check_params(k, T, tk, tp) == REQ_OK;
+    std::vector<int32_t> tok(k);
+    std::vector<double> q(k, nan), mc(k, kInf), mt(k, kInf);
+    for (int i = 0; ok && i < k; ++i) {
+      std::vector<double> x = load_row(logits, dtype, d0 + i, stride, vocab);
+      if (row_has_bad_value(x)) {
+        ok = false;
+        break;
+      }
+      if (T == 0.0f) {
+        tok[i] = argmax_first(x);
+        continue;
+      }
+      std::vector<double> p;
+      if (!row_distribution(x, (double)T, tk, (double)tp, p, &mt[i])) {
+        ok = false;
+        break;
+      }
+      tok[i] = inverse_cdf(p, (double)uniforms[d0 + i], &mc[i]);
+      q[i] = p[tok[i]];
+    }
+    if (!ok) {
+      fail_rows(d0, k);
+    } else {
+      for (int i = 0; i < k; ++i) {
+        out_tokens[d0 + i] = tok[i];
+        if (out_q) out_q[d0 + i] = q[i];
+        if (out_margins) {
+          out_margins[2 * (d0 + i)] = mc[i];
+          out_margins[2 * (d0 + i) + 1] = mt[i];
+        }
+      }
+    }
+    d0 += k;
+  }
   return OR_OK;
 }
 
