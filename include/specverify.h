@@ -197,6 +197,39 @@ int spec_verify_noalloc(const sv_logits* target_logits, const sv_logits* draft_l
  * allocation-free call. */
 int spec_verify_noalloc_scratch(void** scratch, size_t* bytes);
 
+/* ---- draft-side sampler ---------------------------------------------------
+ * The drafter's token choice that produces the drafts verified above
+ * ("FlashMap: Flow Map Speculative Decoding…", §5 draft_block step 5: logits
+ * divided by the temperature, softmax, a multinomial draw; the argmax at
+ * temperature 0), for a batch of drafter rows laid out like spec_verify's
+ * draft rows: request b owns rows d_off[b] .. d_off[b] + k_b - 1 with
+ * d_off[b] = sum_{j<b} k_j.
+ *   Row i of request b draws x_i = min{ y : C_y > u_i * S } by inverse CDF in
+ *   vocabulary-index order over the row's distribution at the request's
+ *   temperature, filtered by its top-k / top-p exactly as spec_verify filters
+ *   p and q (so the q that verification recomputes is the one drawn from);
+ *   temperature 0 takes the argmax of the raw logits, lowest index on ties.
+ *   draft_logits  [R, V], R = sum_b k_b; same alignment rules as spec_verify
+ *   k_per_req     [B] int32, 0 .. SV_MAX_K
+ *   temperature   [B] float, 0 = greedy
+ *   top_k, top_p  [B] or NULL, as in spec_verify
+ *   uniforms      [R] float in [0, 1): row d_off[b] + i draws with u_i
+ *   out_tokens    [R] int32: x_i; -1 for every row of a request with a data
+ *                 error (bad parameters, NaN / +inf logit)
+ *   out_q         [R] float or NULL: q_i(x_i), the drawn token's probability
+ *                 (NaN for greedy and failed rows)
+ *   workspace     >= spec_draft_sample_workspace_size(B, R) bytes, 256-byte
+ *                 aligned, owned by the caller
+ * Same ownership, stream and error conventions as spec_verify (errors are read
+ * back with spec_verify_get_error on this workspace).  Returns SV_OK once the
+ * work is enqueued, else an SV_ERR_* code. */
+size_t spec_draft_sample_workspace_size(int32_t batch, int64_t rows);
+
+int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
+                      const float* temperature, const int32_t* top_k, const float* top_p,
+                      const float* uniforms, int32_t* out_tokens, float* out_q, void* stream,
+                      int32_t batch, void* workspace, size_t workspace_bytes);
+
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);
 

@@ -27,7 +27,7 @@ import torch
 
 __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
            "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
-           "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES"]
+           "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -100,6 +100,11 @@ def load_library():
             lib.spec_verify_strerror.argtypes = [ctypes.c_int]
             lib.spec_verify_version.restype = ctypes.c_int
             lib.spec_verify_version.argtypes = []
+            lib.spec_draft_sample_workspace_size.restype = sz
+            lib.spec_draft_sample_workspace_size.argtypes = [i32, i64]
+            lib.spec_draft_sample.restype = ctypes.c_int
+            lib.spec_draft_sample.argtypes = [ctypes.POINTER(_Logits), P, P, P, P, P, P, P, P,
+                                              i32, P, sz]
             _lib = lib
     return _lib
 
@@ -225,7 +230,66 @@ class Verifier:
         return dump_rows(self.workspace, batch, target_rows, draft_rows, stream)
 
 
+class DraftSampler:
+    """Draft-side sampler (the drafter's token choice whose drafts Verifier
+    checks): x_i drawn from the temperature softmax of drafter row i, filtered
+    by the request's top-k / top-p as verification filters, by inverse CDF in
+    index order with u_i; argmax at temperature 0.  Rows are laid out like the
+    verifier's draft rows.  One DraftSampler per stream."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.workspace = None
+
+    def _workspace(self, B, R):
+        need = int(load_library().spec_draft_sample_workspace_size(int(B), int(R)))
+        if need == 0 and (B or R):
+            raise SpecVerifyError(1, "spec_draft_sample_workspace_size")
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self.workspace
+
+    def __call__(self, logits, k_per_req, temperature, uniforms, top_k=None, top_p=None, *,
+                 out_tokens=None, out_q=None, with_q=False, stream=None):
+        """Returns ``(tokens [R] int32, q [R] float32 or None)`` on the device."""
+        lib = load_library()
+        B = int(k_per_req.shape[0])
+        _check(k_per_req, "k_per_req", torch.int32)
+        _check(temperature, "temperature", torch.float32)
+        _check(uniforms, "uniforms", torch.float32)
+        _check(top_k, "top_k", torch.int32)
+        _check(top_p, "top_p", torch.float32)
+        xd = _logits_desc(logits)
+        R = int(xd.rows)
+        if out_tokens is None:
+            out_tokens = torch.empty(R, dtype=torch.int32, device=logits.device)
+        _check(out_tokens, "out_tokens", torch.int32)
+        if out_q is None and with_q:
+            out_q = torch.empty(R, dtype=torch.float32, device=logits.device)
+        _check(out_q, "out_q", torch.float32)
+        ws = self._workspace(B, R)
+        rc = lib.spec_draft_sample(ctypes.byref(xd), _ptr(k_per_req), _ptr(temperature),
+                                   _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
+                                   _ptr(out_q), _stream_handle(stream), B, _ptr(ws), ws.numel())
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_draft_sample")
+        return out_tokens, out_q
+
+    def error(self, stream=None):
+        return get_error(self.workspace, stream)
+
+
 _default = {}
+_default_sampler = {}
+
+
+def draft_sample(logits, k_per_req, temperature, uniforms, top_k=None, top_p=None, **kw):
+    """One-shot draft-side sampling with a per-device cached DraftSampler."""
+    dev = logits.device
+    s = _default_sampler.get(dev)
+    if s is None:
+        s = _default_sampler[dev] = DraftSampler(dev)
+    return s(logits, k_per_req, temperature, uniforms, top_k, top_p, **kw)
 
 
 def verify(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k=None,

@@ -1,6 +1,7 @@
 // Host side of the C ABI: argument validation, workspace layout, and the
-// four launches (setup -> row pass -> filter / decide -> draw pass) on the
-// caller's stream.
+// four launches on the caller's stream: setup -> row pass -> filter / decide
+// -> draw pass for verification, sampler setup -> row pass -> sampler rows ->
+// draw pass for the draft-side sampler.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -129,6 +130,8 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   P.out_accept_len = out_accept_len;
   P.out_tokens = out_tokens;
   P.out_pq = options ? options->out_pq : nullptr;
+  P.out_q = nullptr;
+  P.n_seg = 1;
   P.ws = ws_bind(workspace, L);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -154,6 +157,77 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
   P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, dmax / std::max(batch, 1))));
   const int64_t djobs = int64_t(batch) * P.n_seg;
+  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+size_t spec_draft_sample_workspace_size(int32_t batch, int64_t rows) {
+  if (batch < 0 || rows < 0 || rows >= INT_MAX) return 0;
+  return sample_ws_layout(batch, rows).total;
+}
+
+int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
+                      const float* temperature, const int32_t* top_k, const float* top_p,
+                      const float* uniforms, int32_t* out_tokens, float* out_q, void* stream,
+                      int32_t batch, void* workspace, size_t workspace_bytes) {
+  if (!draft_logits || batch < 0) return SV_ERR_ARG;
+  const sv_logits& x = *draft_logits;
+  if (x.dtype != SV_F32 && x.dtype != SV_BF16) return SV_ERR_UNSUPPORTED;
+  if (x.vocab < 1) return SV_ERR_ARG;
+  if (x.vocab > SV_VOCAB_MAX) return SV_ERR_UNSUPPORTED;
+  if (x.rows < 0 || x.rows >= INT_MAX || x.row_stride < x.vocab) return SV_ERR_ARG;
+  if (batch > 0 && (!k_per_req || !temperature)) return SV_ERR_ARG;
+  if (x.rows > 0 && (!x.data || !uniforms || !out_tokens)) return SV_ERR_ARG;
+  const size_t es = elem_size(x.dtype);
+  if (x.data && (misaligned(x.data, 16) || (size_t(x.row_stride) * es) % 16 != 0))
+    return SV_ERR_UNSUPPORTED;
+  const WsLayout L = sample_ws_layout(batch, x.rows);
+  if (!workspace || misaligned(workspace, 256) || workspace_bytes < L.total)
+    return SV_ERR_WORKSPACE;
+  if (batch == 0) return x.rows == 0 ? SV_OK : SV_ERR_ARG;
+
+  DeviceState ds;
+  if (int rc = prepare_device(x.vocab, &ds)) return rc;
+  const int sms = ds.sms;
+
+  Problem P;
+  P.target = x.data;
+  P.draft = nullptr;
+  P.t_stride = x.row_stride;
+  P.d_stride = 0;
+  P.Rt = x.rows;  // the drafter rows play the part of target rows in the row pass
+  P.Rd = 0;
+  P.V = x.vocab;
+  P.B = batch;
+  P.n_seg = 1;
+  P.draft_tokens = nullptr;
+  P.k_per_req = k_per_req;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.uniforms = uniforms;
+  P.out_accept_len = nullptr;
+  P.out_tokens = out_tokens;
+  P.out_pq = nullptr;
+  P.out_q = out_q;
+  P.ws = ws_bind(workspace, L);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_sample_setup(P, s) != cudaSuccess) return SV_ERR_CUDA;
+  const int64_t rows = x.rows;
+  if (rows == 0) return SV_OK;
+  const bool bf16 = x.dtype == SV_BF16;
+  const int64_t ctas = int64_t(sms) * kRowpassCtasPerSm;
+  if (launch_rowpass(P, bf16, int(rows < ctas ? rows : ctas), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  const int64_t fmax = int64_t(sms) * ds.occ_filter;
+  if (launch_sample_post(P, bf16, int(rows < fmax ? rows : fmax), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  // every sampled unfiltered row may queue a draw
+  const int64_t dmax = int64_t(sms) * ds.occ_draw;
+  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, dmax / rows)));
+  const int64_t djobs = rows * P.n_seg;
   if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;

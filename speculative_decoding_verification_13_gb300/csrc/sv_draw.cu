@@ -456,6 +456,10 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
       if (lane == 0) {
         if (y < 0) record_error(w.hdr, SV_ERR_INTERNAL, -1, d.tr);  // no mass found
         P.out_tokens[d.t0 + d.L] = y;
+        if (P.out_q)  // draft sampler: the drawn token's probability (a bonus-kind draw)
+          P.out_q[d.t0 + d.L] =
+              y >= 0 ? ex2_approx((Elt<BF16>::one(trow, y) - d.mt) * d.c2) * d.ist
+                     : __int_as_float(0x7fc00000);
       }
     }
     draw_sync();  // tile sums are rewritten by the next unit

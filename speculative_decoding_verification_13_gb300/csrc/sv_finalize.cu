@@ -769,7 +769,10 @@ __device__ __forceinline__ unsigned long long fix_prob(float p) {
 // summed exactly in fixed point (multiples of 2^-55), so the order of the
 // additions does not matter; C_y is each token's own prefix, summed directly
 // rather than after an index sort.  One warp; warp-uniform result.
-__device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double u, PostShared& sh) {
+// sidx / sr: kFastDraw entries of scratch (shared memory); *qy (if given)
+// receives the drawn token's probability in t (the kept probability itself).
+__device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double u, int* sidx,
+                                      unsigned long long* sr, float* qy) {
   const int lane = threadIdx.x & 31;
   const int Kt = t.kp, Kd = d ? d->kp : 0;
   int idx[2];
@@ -794,15 +797,15 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
       const int j = s * 32 + lane;
       const unsigned long long fp = fix_prob(p[s]), fq = residual ? fix_prob(q[s]) : 0ull;
       if (j < Kt) {
-        sh.idx[j] = idx[s];
-        sh.r[j] = fp > fq ? fp - fq : 0ull;
+        sidx[j] = idx[s];
+        sr[j] = fp > fq ? fp - fq : 0ull;
       }
     }
     __syncwarp();
     unsigned long long C[2] = {0ull, 0ull}, rmine[2] = {0ull, 0ull};
     for (int i = 0; i < Kt; ++i) {
-      const int ii = sh.idx[i];
-      const unsigned long long ri = sh.r[i];
+      const int ii = sidx[i];
+      const unsigned long long ri = sr[i];
 #pragma unroll
       for (int s = 0; s < 2; ++s) {
         if (ii <= idx[s]) C[s] += ri;
@@ -829,7 +832,16 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
     }
     y = __reduce_min_sync(kFull, y);
     last = __reduce_max_sync(kFull, last);
-    return y != INT_MAX ? y : last;  // rounding left no C above u S: the last token with mass
+    y = y != INT_MAX ? y : last;  // rounding left no C above u S: the last token with mass
+    if (qy) {
+      float pv = 0.f;
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+        if (idx[s] == y) pv = p[s];
+      const uint32_t hb = __ballot_sync(kFull, pv != 0.f);
+      *qy = hb ? __shfl_sync(kFull, pv, __ffs(hb) - 1) : 0.f;
+    }
+    return y;
   }
   return -1;  // not reached: the second attempt always returns
 }
@@ -899,7 +911,7 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
     const WarpSel& ts = scr[tw].sel;
     int y;
     if (ts.fast && (!residual || scr[tw + 1].sel.fast))
-      y = draw_fast(ts, residual ? &scr[tw + 1].sel : nullptr, u, sh);
+      y = draw_fast(ts, residual ? &scr[tw + 1].sel : nullptr, u, sh.idx, sh.r, nullptr);
     else
       y = draw_kept(P, t0 + L, P.Rt + d0 + L, residual, u, scr[0].draw);
     for (int i = lane; i <= k; i += 32)
@@ -952,7 +964,96 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
   }
 }
 
+// Draft sampler, after the row pass: one warp per drafter row, rows handed out
+// by a counter.  Greedy rows emit the argmax; filtered rows take the exact
+// top k, the softmax and top-p (the verifier's row filter) and draw from the
+// kept set by inverse CDF in index order with the row's uniform; the other
+// sampled rows are queued for the draw pass, which streams the row again.
+template <bool BF16>
+__global__ void __launch_bounds__(kPostThreads, 2) sample_post_kernel(const Problem P) {
+  extern __shared__ __align__(16) unsigned char post_smem[];
+  WarpScratch* scr = reinterpret_cast<WarpScratch*>(post_smem);
+  const Ws& w = P.ws;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();     // the row pass's results
+  pdl_trigger();  // the draw pass may launch; it waits for this kernel
+  if (w.hdr->global_err) {
+    // batch-level data error: every output is -1 (NaN for q)
+    const int64_t stride = int64_t(gridDim.x) * kPostThreads;
+    for (int64_t r = int64_t(blockIdx.x) * kPostThreads + threadIdx.x; r < P.Rt; r += stride) {
+      P.out_tokens[r] = -1;
+      if (P.out_q) P.out_q[r] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  const int n = w.hdr->n_active;
+  WarpScratch& ws = scr[warp];
+  for (;;) {
+    int j = 0;
+    if (lane == 0) j = atomicAdd(&w.hdr->next_row, 1);
+    j = __shfl_sync(kFull, j, 0);
+    if (j >= n) break;
+    const RowJob job = w.rowlist[j];
+    const int64_t row = job.row;
+    const int mode = job.mode & 3;
+    const double u = double(P.uniforms[row]);
+    int y = -1;
+    float qy = __int_as_float(0x7fc00000);
+    bool queued = false;
+    if (w.req_flag[job.b]) {
+      // a logit error found by the row pass: the request's rows fail
+    } else if (mode == kArgmax) {
+      y = __ldcg(&w.stats[row].arg);
+    } else if (mode == kTopk) {
+      const float tp = P.top_p ? P.top_p[job.b] : 1.0f;
+      warp_filter_row<BF16>(P, row, job.K, job.T, tp, -1, ws.sel);
+      if (ws.sel.fast) {
+        y = draw_fast(ws.sel, nullptr, u, ws.sel.hw, ws.sel.before, &qy);
+      } else {
+        y = draw_kept(P, row, 0, false, u, ws.draw);
+        // the drawn token's kept probability, from the kept list in global memory
+        const int kp = __ldcg(&w.stats[row].kept);
+        float pv = 0.f;
+        for (int i = lane; i < kp; i += 32)
+          if (__ldcg(&w.cand_idx[size_t(row) * kTopkMax + i]) == y)
+            pv = __ldcg(&w.cand_p[size_t(row) * kTopkMax + i]);
+        const uint32_t hb = __ballot_sync(kFull, pv != 0.f);
+        qy = hb ? __shfl_sync(kFull, pv, __ffs(hb) - 1) : 0.f;
+      }
+      __syncwarp();  // the scratch is rewritten by the warp's next row
+    } else {
+      queued = true;
+      if (lane == 0) {
+        const RowStat st = w.stats[row];
+        DrawDesc d;
+        d.tr = row;
+        d.dr = 0;
+        d.mt = st.m;
+        d.ist = float(1.0 / st.s);
+        d.md = 0.f;
+        d.isd = 0.f;
+        d.c2 = __fdiv_rn(1.4426950408889634f, job.T);
+        d.kind = 0;
+        d.u = u;
+        d.t0 = int32_t(row);
+        d.L = 0;
+        w.draw[atomicAdd(&w.hdr->n_draw, 1)] = d;
+      }
+    }
+    if (!queued && lane == 0) {
+      P.out_tokens[row] = y;
+      if (P.out_q) P.out_q[row] = qy;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_sample_post(const Problem& P, bool bf16, int grid, cudaStream_t s) {
+  const size_t smem = sizeof(WarpScratch) * kWarps;
+  if (bf16) return launch_after(sample_post_kernel<true>, grid, kPostThreads, smem, s, P);
+  return launch_after(sample_post_kernel<false>, grid, kPostThreads, smem, s, P);
+}
 
 size_t filter_smem_bytes() { return sizeof(WarpScratch) * kWarps; }
 
@@ -971,6 +1072,12 @@ cudaError_t filter_occupancy(int* occ) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(filter_decide_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sample_post_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(sample_post_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   int a = 0, b = 0;
   if (e == cudaSuccess)

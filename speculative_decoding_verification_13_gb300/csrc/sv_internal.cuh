@@ -40,7 +40,8 @@ struct WsHeader {
   int32_t n_filtered;   // filtered requests listed by the setup kernel
   int32_t n_decide;     // other requests listed by the setup kernel
   int32_t n_draw;       // requests queued for the unfiltered draw
-  int32_t pad[7];
+  int32_t next_row;     // draft sampler: rows handed out to warps so far
+  int32_t pad[6];
 };
 
 struct RowStat {
@@ -119,6 +120,12 @@ inline WsLayout ws_layout(int64_t B, int64_t Rt, int64_t Rd) {
   return L;
 }
 
+// Draft sampler: per-queue arrays hold one entry per row (every sampled row
+// may queue a draw), per-request arrays one per request.
+inline WsLayout sample_ws_layout(int64_t B, int64_t R) {
+  return ws_layout(B > R ? B : R, R, 0);
+}
+
 inline Ws ws_bind(void* base, const WsLayout& L) {
   char* p = static_cast<char*>(base);
   Ws w;
@@ -155,6 +162,7 @@ struct Problem {
   int32_t* out_accept_len;
   int32_t* out_tokens;
   double* out_pq;               // may be null
+  float* out_q;                 // draft sampler: q(x) of each drawn token, may be null
   Ws ws;
 };
 
@@ -163,6 +171,8 @@ cudaError_t launch_setup(const Problem& P, cudaStream_t s);
 cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
+cudaError_t launch_sample_post(const Problem& P, bool bf16, int grid, cudaStream_t s);
 size_t rowpass_smem_bytes();
 
 // Launch of a kernel that may start while the previous kernel on the stream

@@ -196,7 +196,106 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   }
 }
 
+// Setup of the draft sampler: one CTA.  Request b owns drafter rows
+// d_off[b] .. d_off[b] + k_b - 1 with d_off[b] = sum_{j<b} k_j (the verifier's
+// draft-row layout).  Validates each request's parameters, writes the row list
+// (every row of a valid request; mode argmax at T = 0, top-k survivors when
+// the request filters, softmax statistics otherwise) and gives the rows of a
+// failed request their outputs (-1, NaN) here.
+__global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Problem P) {
+  const Ws& w = P.ws;
+  __shared__ int s_bad;
+  pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
+  if (threadIdx.x == 0) {
+    w.hdr->err_code = 0;
+    w.hdr->err_req = -1;
+    w.hdr->err_row = -1;
+    w.hdr->n_active = 0;
+    w.hdr->global_err = 0;
+    w.hdr->n_filtered = 0;
+    w.hdr->n_decide = 0;
+    w.hdr->n_draw = 0;
+    w.hdr->next_row = 0;
+    s_bad = 0;
+  }
+  // every row may queue a draw: their segment counters start at zero
+  for (int64_t q = threadIdx.x; q < P.Rt; q += kSetupThreads) w.seg_cnt[q] = 0;
+  __syncthreads();
+
+  // Pass 1: row offsets; a k outside [0, SV_MAX_K] makes the layout undefined.
+  int carry = 0;
+  for (int base = 0; base < P.B; base += kSetupThreads) {
+    const int b = base + threadIdx.x;
+    int k = 0;
+    if (b < P.B) {
+      k = P.k_per_req[b];
+      if (k < 0 || k > SV_MAX_K) {
+        record_error(w.hdr, SV_ERR_DATA_K, b, -1);
+        atomicOr(&s_bad, 1);
+        k = 0;
+      }
+    }
+    unsigned long long tot;
+    const unsigned long long ex = block_exclusive_scan(b < P.B ? pack2(uint32_t(k), 0u) : 0ull, &tot);
+    if (b < P.B) w.t_off[b] = carry + int(uint32_t(ex));
+    carry += int(uint32_t(tot));
+  }
+  if (threadIdx.x == 0) {
+    w.t_off[P.B] = carry;
+    if (!s_bad && carry != P.Rt) {
+      record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
+      s_bad = 1;
+    }
+    if (s_bad) w.hdr->global_err = 1;
+  }
+  __syncthreads();
+  if (s_bad) return;
+
+  // Pass 2: per-request validation, modes and the row list.
+  int carry_a = 0;
+  for (int base = 0; base < P.B; base += kSetupThreads) {
+    const int b = base + threadIdx.x;
+    int code = 0, active = 0, mode = kSkip, k = 0, d0 = 0, tk = 0;
+    float T = 0.f;
+    if (b < P.B) {
+      k = P.k_per_req[b];
+      d0 = w.t_off[b];
+      T = P.temperature[b];
+      const float tp = P.top_p ? P.top_p[b] : 1.0f;
+      tk = P.top_k ? P.top_k[b] : 0;
+      const bool topk_on = tk > 0 && tk < P.V;
+      const bool filtered = T > 0.0f && (topk_on || tp < 1.0f);
+      if (!(T >= 0.0f) || isinf(T)) code = SV_ERR_DATA_TEMPERATURE;
+      else if (!(tp > 0.0f && tp <= 1.0f)) code = SV_ERR_DATA_TOP_P;
+      else if (tk < 0) code = SV_ERR_DATA_TOP_K;
+      else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
+      w.req_flag[b] = code;
+      if (code) {
+        record_error(w.hdr, code, b, -1);
+        for (int i = 0; i < k; ++i) {
+          P.out_tokens[d0 + i] = -1;
+          if (P.out_q) P.out_q[d0 + i] = __int_as_float(0x7fc00000);
+        }
+      } else {
+        mode = T == 0.0f ? kArgmax : (filtered ? kTopk : kStats);
+        active = k;
+      }
+    }
+    unsigned long long tot;
+    const int a0 = carry_a + int(uint32_t(block_exclusive_scan(uint32_t(active), &tot)));
+    carry_a += int(uint32_t(tot));
+    for (int i = 0; i < active; ++i)
+      w.rowlist[a0 + i] = RowJob{d0 + i, b, -1, (i << 2) | mode, T, tk, {0, 0}};
+  }
+  if (threadIdx.x == 0) w.hdr->n_active = carry_a;
+}
+
 }  // namespace
+
+cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s) {
+  sample_setup_kernel<<<1, kSetupThreads, 0, s>>>(P);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_setup(const Problem& P, cudaStream_t s) {
   setup_kernel<<<1, kSetupThreads, 0, s>>>(P);

@@ -1,0 +1,134 @@
+"""Draft-side sampler on the GPU against the oracle, element by element on the
+same seeded rows and uniforms: tokens bit-exact except where the oracle's own
+decision margin is below the rounding of a float implementation (CDF margin
+< 1e-5, top-p margin < 1e-12), q(x) within the probability tolerance."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_13_gb300 as sv
+from speculative_decoding_verification_13_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def sample_case(name, k, T, V, dtype, seed, top_k=None, top_p=None, sigma=1.0):
+    """Drafter rows (the draft rows of a synthetic batch) and fresh uniforms."""
+    B = len(k)
+    b = W.make_batch_from_params(name, k, T, [sigma] * B, V, dtype, seed, device=DEV,
+                                 top_k=top_k, top_p=top_p)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed + 7)
+    u = torch.rand(b.draft_rows, generator=g, device=DEV)
+    return b.draft, b.k_per_req, b.temperature, b.top_k, b.top_p, u
+
+
+def check(case, name, threads=16):
+    x, k, T, tk, tp, u = case
+    s = sv.DraftSampler(DEV)
+    tok, q = s(x, k, T, u, tk, tp, with_q=True)
+    torch.cuda.synchronize()
+    code = s.error()[0]
+    o = oracle.draft_sample(x.cpu(), k.cpu(), T.cpu(), u.cpu(), tk.cpu(), tp.cpu(),
+                            threads=threads)
+    tok, q = tok.cpu().numpy(), q.cpu().numpy()
+    R = tok.shape[0]
+    exempt = (o["margins"][:, 0] < 1e-5) | (o["margins"][:, 1] < 1e-12)
+    mism = tok != o["tokens"]
+    bad = np.nonzero(mism & ~exempt)[0]
+    print(f"{name}: {R} rows, exempt {int(exempt.sum())}, mismatches non-exempt {len(bad)} "
+          f"exempt {int((mism & exempt).sum())}")
+    assert len(bad) == 0, f"non-exempt mismatches at rows {bad[:10]}"
+    same = ~mism
+    tol = 2e-3 if x.dtype == torch.bfloat16 else 1e-5
+    oq = o["q"][same]
+    gq = q[same]
+    nan = np.isnan(oq)
+    assert (np.isnan(gq) == nan).all(), "q NaN pattern"
+    if (~nan).any():
+        rel = np.abs(gq[~nan] - oq[~nan]) / np.maximum(oq[~nan], 1e-30)
+        assert rel.max() <= tol, f"q rel err {rel.max()}"
+    return code, tok, o
+
+
+def test_mixed_small_fp32():
+    k = [3, 0, 5, 1, 4, 2, 5, 3, 0, 2, 4, 1]
+    T = [1.0, 1.0, 0.7, 0.0, 1.2, 0.0, 0.9, 1.0, 0.5, 1.3, 0.8, 1.0]
+    tk = [0, 0, 20, 0, 64, 5, 1, 256, 0, 100, 0, 50]  # top-p needs top-k on the boundary
+    tp = [1.0, 1.0, 0.9, 1.0, 0.6, 1.0, 1.0, 1.0, 1.0, 0.95, 1.0, 0.8]
+    code, _, _ = check(sample_case("mixed", k, T, 1000, torch.float32, 31, tk, tp), "mixed")
+    assert code == 0
+
+
+def test_c4_shape_filtered_bf16():
+    """The bench workload's drafter rows: top-k 50, top-p 0.9, T = 1 (64 requests)."""
+    B = 64
+    code, _, _ = check(sample_case("c4 sampler", [15] * B, [1.0] * B, W.VOCAB_QWEN3,
+                                   torch.bfloat16, 32, [50] * B, [0.9] * B), "c4-shape filtered")
+    assert code == 0
+
+
+def test_unfiltered_bf16_draws_through_the_draw_pass():
+    B = 16
+    code, _, _ = check(sample_case("unfiltered", [15] * B, [1.0] * 8 + [0.6] * 8,
+                                   W.VOCAB_QWEN3, torch.bfloat16, 33), "unfiltered")
+    assert code == 0
+
+
+def test_greedy_rows_are_the_argmax():
+    B = 20
+    x, k, T, tk, tp, u = sample_case("greedy", [4] * B, [0.0] * B, 32000, torch.float32, 34)
+    tok, q = sv.draft_sample(x, k, T, u, with_q=True)
+    assert torch.equal(tok.long(), torch.argmax(x, dim=1))
+    assert torch.isnan(q).all()
+
+
+def test_large_kept_sets_take_the_general_draw():
+    """top-k 256 with top-p off keeps more than 64 tokens: the kept-list draw."""
+    B = 6
+    code, _, _ = check(sample_case("k256", [5] * B, [1.5] * B, 50000, torch.bfloat16, 35,
+                                   [256] * B, [1.0] * B), "top-k 256")
+    assert code == 0
+
+
+def test_data_errors_fail_their_requests_only():
+    k = [2, 3, 2, 1]
+    x, kk, T, tk, tp, u = sample_case("errors", k, [1.0, 1.0, 0.8, 1.0], 500, torch.float32, 36)
+    x = x.clone()
+    x[3, 17] = float("nan")                       # request 1 (rows 2..4)
+    T = T.clone()
+    T[3] = -1.0                                    # request 3 (row 7)
+    s = sv.DraftSampler(DEV)
+    tok, q = s(x, kk, T, u, with_q=True)
+    code = s.error()[0]
+    tok = tok.cpu().numpy()
+    assert (tok[2:5] == -1).all() and tok[7] == -1
+    assert torch.isnan(q[2:5]).all() and torch.isnan(q[7])
+    o = oracle.draft_sample(x.cpu(), kk.cpu(), T.cpu(), u.cpu())
+    assert (tok == o["tokens"]).all()
+    assert code != 0
+
+
+def test_row_count_mismatch_fails_the_batch():
+    x, k, T, tk, tp, u = sample_case("rows", [3, 3], [1.0, 1.0], 300, torch.float32, 37)
+    s = sv.DraftSampler(DEV)
+    tok, _ = s(x[:5].contiguous(), k, T, u[:5].contiguous())
+    assert (tok.cpu() == -1).all()
+    assert s.error()[0] == 21
+
+
+def test_empty_and_k_zero_batches():
+    s = sv.DraftSampler(DEV)
+    x = torch.zeros(0, 100, dtype=torch.float32, device=DEV)
+    k = torch.zeros(3, dtype=torch.int32, device=DEV)
+    T = torch.ones(3, dtype=torch.float32, device=DEV)
+    u = torch.zeros(0, dtype=torch.float32, device=DEV)
+    tok, _ = s(x, k, T, u)
+    torch.cuda.synchronize()
+    assert tok.numel() == 0
+    tok, _ = s(x, k[:0], T[:0], u)
+    assert tok.numel() == 0
