@@ -220,6 +220,7 @@ int spec_verify_noalloc_scratch(void** scratch, size_t* bytes);
  *                 (NaN for greedy and failed rows)
  *   workspace     >= spec_draft_sample_workspace_size(B, R) bytes, 256-byte
  *                 aligned, owned by the caller
+ *   options       NULL, or row-pass events as in spec_verify (out_pq ignored)
  * Same ownership, stream and error conventions as spec_verify (errors are read
  * back with spec_verify_get_error on this workspace).  Returns SV_OK once the
  * work is enqueued, else an SV_ERR_* code. */
@@ -228,7 +229,8 @@ size_t spec_draft_sample_workspace_size(int32_t batch, int64_t rows);
 int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
                       const float* temperature, const int32_t* top_k, const float* top_p,
                       const float* uniforms, int32_t* out_tokens, float* out_q, void* stream,
-                      int32_t batch, void* workspace, size_t workspace_bytes);
+                      int32_t batch, void* workspace, size_t workspace_bytes,
+                      const sv_options* options);
 
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);

@@ -104,7 +104,7 @@ def load_library():
             lib.spec_draft_sample_workspace_size.argtypes = [i32, i64]
             lib.spec_draft_sample.restype = ctypes.c_int
             lib.spec_draft_sample.argtypes = [ctypes.POINTER(_Logits), P, P, P, P, P, P, P, P,
-                                              i32, P, sz]
+                                              i32, P, sz, ctypes.POINTER(_Options)]
             _lib = lib
     return _lib
 
@@ -250,7 +250,7 @@ class DraftSampler:
         return self.workspace
 
     def __call__(self, logits, k_per_req, temperature, uniforms, top_k=None, top_p=None, *,
-                 out_tokens=None, out_q=None, with_q=False, stream=None):
+                 out_tokens=None, out_q=None, with_q=False, stream=None, rowpass_events=None):
         """Returns ``(tokens [R] int32, q [R] float32 or None)`` on the device."""
         lib = load_library()
         B = int(k_per_req.shape[0])
@@ -268,9 +268,14 @@ class DraftSampler:
             out_q = torch.empty(R, dtype=torch.float32, device=logits.device)
         _check(out_q, "out_q", torch.float32)
         ws = self._workspace(B, R)
+        opts = None
+        if rowpass_events is not None:
+            ev0, ev1 = rowpass_events
+            opts = _Options(None, _event_handle(ev0, stream), _event_handle(ev1, stream))
         rc = lib.spec_draft_sample(ctypes.byref(xd), _ptr(k_per_req), _ptr(temperature),
                                    _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
-                                   _ptr(out_q), _stream_handle(stream), B, _ptr(ws), ws.numel())
+                                   _ptr(out_q), _stream_handle(stream), B, _ptr(ws), ws.numel(),
+                                   ctypes.byref(opts) if opts is not None else None)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_draft_sample")
         return out_tokens, out_q

@@ -170,7 +170,8 @@ size_t spec_draft_sample_workspace_size(int32_t batch, int64_t rows) {
 int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
                       const float* temperature, const int32_t* top_k, const float* top_p,
                       const float* uniforms, int32_t* out_tokens, float* out_q, void* stream,
-                      int32_t batch, void* workspace, size_t workspace_bytes) {
+                      int32_t batch, void* workspace, size_t workspace_bytes,
+                      const sv_options* options) {
   if (!draft_logits || batch < 0) return SV_ERR_ARG;
   const sv_logits& x = *draft_logits;
   if (x.dtype != SV_F32 && x.dtype != SV_BF16) return SV_ERR_UNSUPPORTED;
@@ -219,7 +220,13 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   if (rows == 0) return SV_OK;
   const bool bf16 = x.dtype == SV_BF16;
   const int64_t ctas = int64_t(sms) * kRowpassCtasPerSm;
+  if (options && options->event_rowpass_begin &&
+      cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
+    return SV_ERR_CUDA;
   if (launch_rowpass(P, bf16, int(rows < ctas ? rows : ctas), s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (options && options->event_rowpass_end &&
+      cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
     return SV_ERR_CUDA;
   const int64_t fmax = int64_t(sms) * ds.occ_filter;
   if (launch_sample_post(P, bf16, int(rows < fmax ? rows : fmax), s) != cudaSuccess)
