@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (small cases for profiling; not a bench line)")
-    ap.add_argument("--path", choices=["verify", "sample"], default="verify",
+    ap.add_argument("--path", choices=["verify", "sample", "kv"], default="verify",
                     help="verify: spec_verify (the headline); sample: the draft-side sampler "
                          "over the same workload's drafter rows")
     return ap.parse_args()
@@ -422,6 +422,129 @@ def run_sampler(args, ws, rank, local):
         pg.destroy_process_group()
 
 
+KV_METRIC = "KV-cache commit GB/s (read + write) after verifying B=256,k=15 (Qwen3-8B-class cache)"
+KV_SHAPE = dict(layers=36, E=1024, S=16)  # 36 layers, 8 KV heads x 128, bf16, 16-token pages
+KV_REPLICAS = 4
+
+
+def run_kv(args, ws, rank, local):
+    """KV-cache commit after one verification of the bench workload: the
+    accept lengths come from spec_verify on that batch; each request appends
+    its last emitted token and its accepted drafts (36 layers x K and V x 1024
+    bf16 = 147 KB per token) to a paged cache at a random offset in its page."""
+    import torch
+    import speculative_decoding_verification_13_gb300 as sv
+    from speculative_decoding_verification_13_gb300 import build as cuda_build
+    from speculative_decoding_verification_13_gb300 import workloads
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0:
+        cuda_build.build()
+    if pg:
+        pg.barrier()
+    sv.load_library()
+    batch = workloads.make_batch(args.config, device=dev, seed_offset=rank, batch=args.batch)
+    acc, _ = sv.verify(batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
+                       batch.temperature, batch.uniforms, batch.top_k, batch.top_p)
+    B, kmax = batch.batch, int(batch.k_per_req.max())
+    layers, E, S = KV_SHAPE["layers"], KV_SHAPE["E"], KV_SHAPE["S"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(1500 + rank)
+    n0 = torch.randint(0, S, (B,), generator=g, device=dev, dtype=torch.int32)
+    per_req = (S - 1 + kmax + 1 + S - 1) // S           # pages a request can touch
+    n_pages = B * per_req
+    table = torch.arange(n_pages, device=dev, dtype=torch.int32).view(B, per_req)
+    table = table[:, torch.randperm(per_req, generator=g, device=dev)].contiguous()
+    # KV_REPLICAS independent caches and speculative buffers, used in turn:
+    # a step touches memory last used KV_REPLICAS - 1 steps (~500 MB) earlier,
+    # so its reads come from HBM, not from the 129 MB L2
+    caches = [torch.empty(n_pages, layers, 2, S, E, dtype=torch.bfloat16, device=dev)
+              for _ in range(KV_REPLICAS)]
+    specs = [torch.randn(B, kmax + 1, layers, 2, E, generator=g, device=dev).to(torch.bfloat16)
+             for _ in range(KV_REPLICAS)]
+    cache, spec = caches[0], specs[0]
+    tokens = int((acc.clamp(min=-1) + 1).sum())
+    bytes_per_step = 2 * tokens * layers * 2 * E * 2      # read and write
+    kv_len = n0.clone()
+    stream = torch.cuda.current_stream(dev)
+    it = [0]
+
+    def step():
+        r = it[0] % KV_REPLICAS
+        it[0] += 1
+        kv_len.copy_(n0)
+        sv.kv_commit(caches[r], specs[r], acc, batch.k_per_req, kv_len, table)
+    clocks = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if sv.kv_commit_error(device=dev)[0] != 0:
+        raise RuntimeError("KV commit data error during warm-up")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    step_ms = max_over_ranks(start.elapsed_time(end) / args.steps, pg, dev)
+    clk = clocks.stop() if clocks else None
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+    peak, peak_src = measured_peak()
+    achieved = bytes_per_step / (step_ms * 1e-3) / 1e9
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        from oracle.kv import kv_commit as oracle_commit
+        import numpy as np
+        c_h = cache.view(torch.int16).cpu().numpy()
+        s_h = spec.view(torch.int16).cpu().numpy()
+        a_h, k_h, n_h, t_h = (t.cpu().numpy() for t in (acc, batch.k_per_req, n0, table))
+        reps = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle_commit(s_h, a_h, k_h, n_h, t_h, c_h, S)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 3.0:
+                break
+        cpu = {"value": reps * bytes_per_step / dt / 1e9, "unit": "GB/s", "cores": 1,
+               "kind": "oracle", "sample": f"the whole step ({tokens} tokens) x {reps}, "
+                                           f"one host thread, {dt:.2f} s wall"}
+    line = {
+        "metric": KV_METRIC, "value": ws * achieved, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (accept lengths from verifying the seeded bench batch; random K/V)",
+        "config": {"workload": f"B={B} commits after k=15 verification, {tokens} tokens, "
+                               f"{layers} layers x K,V x {E} bf16 per token, {S}-token pages",
+                   "tokens_per_step": tokens, "bytes_per_step": bytes_per_step,
+                   "l2": f"{KV_REPLICAS} cache / buffer replicas used in turn (each step's "
+                         f"data last touched {KV_REPLICAS - 1} steps earlier), no flush",
+                   "parallelism": f"replicas x{ws} (independent batches)"},
+        "roofline": {"bound": "hbm", "kernel": "kv_copy_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
+                     "note": "timed over whole calls (validation + copy + kv_len reset)"},
+        "e2e": None,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
@@ -430,6 +553,9 @@ def main():
         return
     if args.path == "sample":
         run_sampler(args, ws, rank, local)
+        return
+    if args.path == "kv":
+        run_kv(args, ws, rank, local)
         return
     import torch
     import speculative_decoding_verification_13_gb300 as sv

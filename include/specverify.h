@@ -79,6 +79,9 @@ extern "C" {
 #define SV_ERR_DATA_NO_DRAFT 23     /* temperature > 0 but draft logits absent   */
 #define SV_ERR_TIMEOUT 24           /* an internal bounded wait expired          */
 #define SV_ERR_INTERNAL 25          /* an internal capacity invariant failed     */
+#define SV_ERR_DATA_ACCEPT 26       /* KV commit: accept length above k_b         */
+#define SV_ERR_DATA_PAGE 27         /* KV commit: a destination page missing from */
+                                    /* the block table, or a negative kv_len      */
 
 /* ---- limits -------------------------------------------------------------- */
 #define SV_MAX_K 32              /* drafts per request (one warp ballot)       */
@@ -231,6 +234,47 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
                       const float* uniforms, int32_t* out_tokens, float* out_q, void* stream,
                       int32_t batch, void* workspace, size_t workspace_bytes,
                       const sv_options* options);
+
+/* ---- KV-cache commit after verification ------------------------------------
+ * The verification stage of the serving pipeline updates the paged KV cache
+ * with the accepted tokens ("FlashMap: Flow Map Speculative Decoding…",
+ * section "Architecture"), and the rollback truncates on rejection
+ * ("Speculative decoding and multi-token prediction", "Practical guidance").
+ * The pages define no layout; this one is chosen:
+ *   cache  [num_pages, n_layers, 2, page_size, E]  (K, then V), E elements of
+ *          elem_bytes each per token per layer
+ *   spec   [B, spec_slots, n_layers, 2, E]: the K/V the verification pass
+ *          wrote for its k_b + 1 inputs, entry 0 the last emitted token (not in
+ *          the cache yet), entries 1..k_b the drafts
+ *   position p of request b lives in page block_table[b * max_pages + p /
+ *   page_size] at slot p % page_size.
+ * With accept length L = accept_len[b] >= 0 (spec_verify's output), entries
+ * 0..L are written to positions kv_len[b] .. kv_len[b] + L and kv_len[b]
+ * grows by L + 1; the entries of rejected drafts are not written.  L = -1 (a
+ * request that failed verification) leaves the request untouched.  A request
+ * with L > k_b (or L + 1 > spec_slots) fails with SV_ERR_DATA_ACCEPT, one
+ * whose destination page is missing (entry < 0 or >= num_pages, or a column
+ * past max_pages) or whose kv_len is negative with SV_ERR_DATA_PAGE: nothing
+ * of a failed request is written and its kv_len is unchanged.  The first data
+ * error is read back with spec_verify_get_error on this workspace.
+ * E * elem_bytes must be a multiple of 16 and both base pointers 16-byte
+ * aligned (SV_ERR_UNSUPPORTED otherwise).  All pointers are device pointers
+ * owned by the caller; the call is asynchronous on `stream`. */
+typedef struct {
+  void* data;
+  int64_t num_pages;
+  int32_t n_layers;
+  int32_t page_size;    /* tokens per page */
+  int32_t entry_elems;  /* E */
+  int32_t elem_bytes;   /* 2 or 4 */
+} sv_kv_cache;
+
+size_t spec_kv_commit_workspace_size(int32_t batch);
+
+int spec_kv_commit(const sv_kv_cache* cache, const void* spec, int32_t spec_slots,
+                   const int32_t* accept_len, const int32_t* k_per_req, int32_t* kv_len,
+                   const int32_t* block_table, int32_t max_pages, void* stream, int32_t batch,
+                   void* workspace, size_t workspace_bytes);
 
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);

@@ -27,7 +27,8 @@ import torch
 
 __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
            "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
-           "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample"]
+           "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample", "kv_commit",
+           "kv_commit_error"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -64,6 +65,12 @@ class _Logits(ctypes.Structure):
 class _Options(ctypes.Structure):
     _fields_ = [("out_pq", ctypes.c_void_p), ("event_rowpass_begin", ctypes.c_void_p),
                 ("event_rowpass_end", ctypes.c_void_p)]
+
+
+class _KvCache(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("num_pages", ctypes.c_int64),
+                ("n_layers", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("entry_elems", ctypes.c_int32), ("elem_bytes", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -105,6 +112,11 @@ def load_library():
             lib.spec_draft_sample.restype = ctypes.c_int
             lib.spec_draft_sample.argtypes = [ctypes.POINTER(_Logits), P, P, P, P, P, P, P, P,
                                               i32, P, sz, ctypes.POINTER(_Options)]
+            lib.spec_kv_commit_workspace_size.restype = sz
+            lib.spec_kv_commit_workspace_size.argtypes = [i32]
+            lib.spec_kv_commit.restype = ctypes.c_int
+            lib.spec_kv_commit.argtypes = [ctypes.POINTER(_KvCache), P, i32, P, P, P, P, i32, P,
+                                           i32, P, sz]
             _lib = lib
     return _lib
 
@@ -286,6 +298,52 @@ class DraftSampler:
 
 _default = {}
 _default_sampler = {}
+
+
+_kv_ws = {}
+
+
+def kv_commit(cache, spec, accept_len, k_per_req, kv_len, block_table, stream=None):
+    """Append the accepted K/V entries after verification (in place).
+
+    cache: [num_pages, n_layers, 2, page_size, E] CUDA tensor (2- or 4-byte
+    elements); spec: [B, spec_slots, n_layers, 2, E], same dtype; accept_len,
+    k_per_req: [B] int32 (accept_len from verify, -1 = leave untouched);
+    kv_len: [B] int32, updated in place; block_table: [B, max_pages] int32."""
+    lib = load_library()
+    for t, n in ((accept_len, "accept_len"), (k_per_req, "k_per_req"), (kv_len, "kv_len")):
+        _check(t, n, torch.int32)
+    _check(block_table, "block_table", torch.int32, ndim=2)
+    if block_table is not None and not block_table.is_contiguous():
+        raise ValueError("block_table must be contiguous")
+    if cache.dim() != 5 or spec.dim() != 5 or not cache.is_contiguous() or not spec.is_contiguous():
+        raise ValueError("cache and spec must be contiguous 5-D tensors")
+    if cache.dtype != spec.dtype or cache.element_size() not in (2, 4):
+        raise TypeError("cache and spec must share a 2- or 4-byte dtype")
+    P_, L_, two, S_, E_ = cache.shape
+    B, slots = int(spec.shape[0]), int(spec.shape[1])
+    if two != 2 or tuple(spec.shape[2:]) != (L_, 2, E_):
+        raise ValueError("spec must be [B, slots, n_layers, 2, E] matching the cache")
+    desc = _KvCache(cache.data_ptr(), P_, L_, S_, E_, cache.element_size())
+    dev = cache.device.index if cache.device.index is not None else torch.cuda.current_device()
+    need = int(lib.spec_kv_commit_workspace_size(B))
+    ws = _kv_ws.get(dev)
+    if ws is None or ws.numel() < need:
+        ws = _kv_ws[dev] = torch.empty(max(need, 256), dtype=torch.uint8, device=cache.device)
+    rc = lib.spec_kv_commit(ctypes.byref(desc), _ptr(spec), slots, _ptr(accept_len),
+                            _ptr(k_per_req), _ptr(kv_len), _ptr(block_table),
+                            int(block_table.shape[1]) if block_table is not None else 0,
+                            _stream_handle(stream), B, _ptr(ws), ws.numel())
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_kv_commit")
+    return kv_len
+
+
+def kv_commit_error(stream=None, device=None):
+    """First data error of the last kv_commit on this device."""
+    d = torch.device(device or "cuda")
+    return get_error(_kv_ws[d.index if d.index is not None else torch.cuda.current_device()],
+                     stream)
 
 
 def draft_sample(logits, k_per_req, temperature, uniforms, top_k=None, top_p=None, **kw):

@@ -240,6 +240,38 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   return SV_OK;
 }
 
+size_t spec_kv_commit_workspace_size(int32_t batch) {
+  return batch < 0 ? 0 : kv_workspace_bytes(batch);
+}
+
+int spec_kv_commit(const sv_kv_cache* cache, const void* spec, int32_t spec_slots,
+                   const int32_t* accept_len, const int32_t* k_per_req, int32_t* kv_len,
+                   const int32_t* block_table, int32_t max_pages, void* stream, int32_t batch,
+                   void* workspace, size_t workspace_bytes) {
+  if (!cache || batch < 0 || spec_slots < 1 || max_pages < 0) return SV_ERR_ARG;
+  const sv_kv_cache& c = *cache;
+  if (c.num_pages < 0 || c.n_layers < 1 || c.page_size < 1 || c.entry_elems < 1 ||
+      (c.elem_bytes != 2 && c.elem_bytes != 4))
+    return SV_ERR_ARG;
+  const int64_t entry_bytes = int64_t(c.entry_elems) * c.elem_bytes;
+  if (entry_bytes % 16 != 0) return SV_ERR_UNSUPPORTED;
+  if (!workspace || misaligned(workspace, 256) || workspace_bytes < kv_workspace_bytes(batch))
+    return SV_ERR_WORKSPACE;
+  if (batch == 0) return SV_OK;
+  if (!c.data || !spec || !accept_len || !k_per_req || !kv_len || (max_pages > 0 && !block_table))
+    return SV_ERR_ARG;
+  if (misaligned(c.data, 16) || misaligned(spec, 16)) return SV_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (launch_kv_commit(c.data, spec, c.num_pages, c.n_layers, c.page_size, entry_bytes,
+                       spec_slots, accept_len, k_per_req, kv_len, block_table, max_pages, batch,
+                       workspace, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 int spec_verify_get_error(const void* workspace, void* stream, int32_t* code, int32_t* request,
                           int64_t* row) {
   if (!workspace || !code) return SV_ERR_ARG;
@@ -308,6 +340,8 @@ const char* spec_verify_strerror(int code) {
     case SV_ERR_DATA_NO_DRAFT: return "temperature > 0 without draft logits";
     case SV_ERR_TIMEOUT: return "internal bounded wait expired";
     case SV_ERR_INTERNAL: return "internal capacity invariant failed";
+    case SV_ERR_DATA_ACCEPT: return "KV commit: accept length above k";
+    case SV_ERR_DATA_PAGE: return "KV commit: destination page missing or negative kv_len";
     default: return "unknown status";
   }
 }

@@ -172,6 +172,12 @@ cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
+size_t kv_workspace_bytes(int32_t B);
+cudaError_t launch_kv_commit(void* cache, const void* spec, int64_t num_pages, int n_layers,
+                             int page_size, int64_t entry_bytes, int spec_slots,
+                             const int32_t* accept_len, const int32_t* k_per_req,
+                             int32_t* kv_len, const int32_t* block_table, int max_pages, int B,
+                             void* workspace, int sms, cudaStream_t s);
 cudaError_t launch_sample_post(const Problem& P, bool bf16, int grid, cudaStream_t s);
 size_t rowpass_smem_bytes();
 
