@@ -276,6 +276,33 @@ int spec_kv_commit(const sv_kv_cache* cache, const void* spec, int32_t spec_slot
                    const int32_t* block_table, int32_t max_pages, void* stream, int32_t batch,
                    void* workspace, size_t workspace_bytes);
 
+/* ---- LM-head GEMM with fused verification statistics ----------------------
+ * The target's logits are its final hidden states times the unembedding
+ * matrix, z = H W^T ("FlashMap: Flow Map Speculative Decoding…", section 1),
+ * and verification needs of each logit row only its softmax statistics at the
+ * row's temperature, its argmax and the logit of its token (§5 draft_block
+ * step 5; §4).  spec_lmhead_stats computes them in the GEMM's epilogue on the
+ * tensor cores (bf16 inputs, f32 accumulation), so the logits never reach
+ * memory.  Per row r, with T_r = temperature[r] (1 is used when it is 0) and
+ * x_r = tokens[r] (or -1):
+ *   out_max[r]    = max_y z[r][y]                         (float)
+ *   out_sum[r]    = sum_y exp((z[r][y] - out_max[r]) / T_r)  (double)
+ *   out_argmax[r] = the first y with z[r][y] = out_max[r]
+ *   out_token[r]  = z[r][x_r], NaN when x_r < 0 or tokens is NULL
+ * so that p_r(x_r) = exp((out_token[r] - out_max[r]) / T_r) / out_sum[r].
+ *   hidden   [rows, d] bf16, row-major, 16-byte aligned, d a multiple of 8
+ *   unembed  [vocab, d] bf16, row-major, 16-byte aligned
+ *   workspace >= spec_lmhead_stats_workspace_size(rows, vocab) bytes
+ * All pointers are device pointers owned by the caller; asynchronous on
+ * `stream`.  A bounded internal wait that expires is recorded as
+ * SV_ERR_TIMEOUT (spec_verify_get_error on this workspace). */
+size_t spec_lmhead_stats_workspace_size(int32_t rows, int32_t vocab);
+
+int spec_lmhead_stats(const void* hidden, const void* unembed, int32_t rows, int32_t vocab,
+                      int32_t d, const float* temperature, const int32_t* tokens,
+                      float* out_max, double* out_sum, int32_t* out_argmax, float* out_token,
+                      void* stream, void* workspace, size_t workspace_bytes);
+
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);
 

@@ -28,7 +28,7 @@ import torch
 __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
            "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
            "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample", "kv_commit",
-           "kv_commit_error"]
+           "kv_commit_error", "lmhead_stats", "lmhead_stats_error"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -112,6 +112,10 @@ def load_library():
             lib.spec_draft_sample.restype = ctypes.c_int
             lib.spec_draft_sample.argtypes = [ctypes.POINTER(_Logits), P, P, P, P, P, P, P, P,
                                               i32, P, sz, ctypes.POINTER(_Options)]
+            lib.spec_lmhead_stats_workspace_size.restype = sz
+            lib.spec_lmhead_stats_workspace_size.argtypes = [i32, i32]
+            lib.spec_lmhead_stats.restype = ctypes.c_int
+            lib.spec_lmhead_stats.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P, P, sz]
             lib.spec_kv_commit_workspace_size.restype = sz
             lib.spec_kv_commit_workspace_size.argtypes = [i32]
             lib.spec_kv_commit.restype = ctypes.c_int
@@ -298,6 +302,50 @@ class DraftSampler:
 
 _default = {}
 _default_sampler = {}
+
+
+_lm_ws = {}
+
+
+def lmhead_stats(hidden, unembed, temperature, tokens=None, stream=None):
+    """Verification statistics of the logits hidden @ unembed.T, computed in the
+    tensor-core GEMM's epilogue (the logits are never stored).  hidden [M, d]
+    and unembed [V, d] bf16 CUDA tensors; temperature [M] float32; tokens [M]
+    int32 or None.  Returns (max [M] f32, sum [M] f64, argmax [M] i32,
+    token logit [M] f32)."""
+    lib = load_library()
+    for t, n in ((hidden, "hidden"), (unembed, "unembed")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 2 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous 2-D bfloat16 CUDA tensor")
+    _check(temperature, "temperature", torch.float32)
+    _check(tokens, "tokens", torch.int32)
+    M, d = hidden.shape
+    V = unembed.shape[0]
+    if unembed.shape[1] != d:
+        raise ValueError("hidden and unembed must share d")
+    dev = hidden.device
+    out_m = torch.empty(M, dtype=torch.float32, device=dev)
+    out_s = torch.empty(M, dtype=torch.float64, device=dev)
+    out_a = torch.empty(M, dtype=torch.int32, device=dev)
+    out_x = torch.empty(M, dtype=torch.float32, device=dev)
+    need = int(lib.spec_lmhead_stats_workspace_size(M, V))
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _lm_ws.get(key)
+    if ws is None or ws.numel() < need:
+        ws = _lm_ws[key] = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    rc = lib.spec_lmhead_stats(_ptr(hidden), _ptr(unembed), M, V, d, _ptr(temperature),
+                               _ptr(tokens), _ptr(out_m), _ptr(out_s), _ptr(out_a), _ptr(out_x),
+                               _stream_handle(stream), _ptr(ws), ws.numel())
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_lmhead_stats")
+    return out_m, out_s, out_a, out_x
+
+
+def lmhead_stats_error(stream=None, device=None):
+    d = torch.device(device or "cuda")
+    return get_error(_lm_ws[d.index if d.index is not None else torch.cuda.current_device()],
+                     stream)
 
 
 _kv_ws = {}

@@ -272,6 +272,33 @@ int spec_kv_commit(const sv_kv_cache* cache, const void* spec, int32_t spec_slot
   return SV_OK;
 }
 
+size_t spec_lmhead_stats_workspace_size(int32_t rows, int32_t vocab) {
+  if (rows < 0 || vocab < 1) return 0;
+  return lmhead_workspace_bytes(rows, vocab);
+}
+
+int spec_lmhead_stats(const void* hidden, const void* unembed, int32_t rows, int32_t vocab,
+                      int32_t d, const float* temperature, const int32_t* tokens,
+                      float* out_max, double* out_sum, int32_t* out_argmax, float* out_token,
+                      void* stream, void* workspace, size_t workspace_bytes) {
+  if (rows < 0 || vocab < 1 || d < 1) return SV_ERR_ARG;
+  if (d % 8 != 0) return SV_ERR_UNSUPPORTED;
+  if (!workspace || misaligned(workspace, 256) ||
+      workspace_bytes < lmhead_workspace_bytes(rows, vocab))
+    return SV_ERR_WORKSPACE;
+  if (rows == 0) return SV_OK;
+  if (!hidden || !unembed || !temperature || !out_max || !out_sum || !out_argmax || !out_token)
+    return SV_ERR_ARG;
+  if (misaligned(hidden, 16) || misaligned(unembed, 16)) return SV_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return launch_lmhead_stats(hidden, unembed, rows, vocab, d, temperature, tokens, out_max,
+                             out_sum, out_argmax, out_token, workspace, sms,
+                             static_cast<cudaStream_t>(stream));
+}
+
 int spec_verify_get_error(const void* workspace, void* stream, int32_t* code, int32_t* request,
                           int64_t* row) {
   if (!workspace || !code) return SV_ERR_ARG;

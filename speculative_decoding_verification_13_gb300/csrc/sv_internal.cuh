@@ -173,6 +173,11 @@ cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStre
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
 size_t kv_workspace_bytes(int32_t B);
+size_t lmhead_workspace_bytes(int M, int V);
+int launch_lmhead_stats(const void* H, const void* W, int M, int V, int K,
+                        const float* temperature, const int32_t* tokens, float* out_m,
+                        double* out_s, int32_t* out_arg, float* out_xt, void* workspace,
+                        int sms, cudaStream_t s);
 cudaError_t launch_kv_commit(void* cache, const void* spec, int64_t num_pages, int n_layers,
                              int page_size, int64_t entry_bytes, int spec_slots,
                              const int32_t* accept_len, const int32_t* k_per_req,
