@@ -303,6 +303,26 @@ int spec_lmhead_stats(const void* hidden, const void* unembed, int32_t rows, int
                       float* out_max, double* out_sum, int32_t* out_argmax, float* out_token,
                       void* stream, void* workspace, size_t workspace_bytes);
 
+/* ---- adaptive speculation length -------------------------------------------
+ * "Speculative decoding and multi-token prediction", section "Acceptance rate
+ * is the whole economics": a drafted position beyond k is worth alpha^k tokens
+ * for a draft step's cost c (a fraction of a target step), so speculation
+ * pays while alpha^k stays above c; alpha varies per request and within a
+ * response.  spec_adapt_k updates, per request, decayed counts of accepted
+ * and rejected positions from the last pass's accept length and picks the next
+ * k, on the stream right after spec_verify:
+ *   succ[b] = decay * succ[b] + L_b,  fail[b] = decay * fail[b] + (L_b < k_b)
+ *   alpha_b = (succ[b] + 1) / (succ[b] + fail[b] + 2)
+ *   k_next[b] = the largest k in [k_min, k_max] with alpha_b^k > c, else k_min
+ * A request with L_b = -1 keeps its counts and k_next[b] = k_used[b].
+ *   accept_len, k_used [B] int32; succ, fail [B] double, in / out (start at 0);
+ *   k_next [B] int32 out; alpha [B] float out or NULL.
+ * 0 <= k_min <= k_max <= SV_MAX_K, 0 <= decay <= 1, c >= 0 (SV_ERR_ARG
+ * otherwise).  Device pointers; asynchronous on `stream`. */
+int spec_adapt_k(const int32_t* accept_len, const int32_t* k_used, double* succ, double* fail,
+                 double decay, double c, int32_t k_min, int32_t k_max, int32_t* k_next,
+                 float* alpha, void* stream, int32_t batch);
+
 /* Human-readable text of a status code. */
 const char* spec_verify_strerror(int code);
 

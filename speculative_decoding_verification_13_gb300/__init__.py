@@ -28,7 +28,8 @@ import torch
 __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "strerror",
            "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
            "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample", "kv_commit",
-           "kv_commit_error", "lmhead_stats", "lmhead_stats_error"]
+           "kv_commit_error", "lmhead_stats", "lmhead_stats_error",
+           "adapt_k"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -116,6 +117,9 @@ def load_library():
             lib.spec_lmhead_stats_workspace_size.argtypes = [i32, i32]
             lib.spec_lmhead_stats.restype = ctypes.c_int
             lib.spec_lmhead_stats.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P, P, sz]
+            lib.spec_adapt_k.restype = ctypes.c_int
+            lib.spec_adapt_k.argtypes = [P, P, P, P, ctypes.c_double, ctypes.c_double, i32, i32,
+                                         P, P, P, i32]
             lib.spec_kv_commit_workspace_size.restype = sz
             lib.spec_kv_commit_workspace_size.argtypes = [i32]
             lib.spec_kv_commit.restype = ctypes.c_int
@@ -302,6 +306,26 @@ class DraftSampler:
 
 _default = {}
 _default_sampler = {}
+
+
+def adapt_k(accept_len, k_used, succ, fail, decay=0.9, c=0.1, k_min=1, k_max=16,
+            with_alpha=False, stream=None):
+    """Next speculation length per request from its measured acceptance
+    (updates succ / fail in place).  Returns (k_next [B] int32, alpha or None)."""
+    lib = load_library()
+    _check(accept_len, "accept_len", torch.int32)
+    _check(k_used, "k_used", torch.int32)
+    _check(succ, "succ", torch.float64)
+    _check(fail, "fail", torch.float64)
+    B = int(accept_len.shape[0])
+    k_next = torch.empty(B, dtype=torch.int32, device=accept_len.device)
+    alpha = torch.empty(B, dtype=torch.float32, device=accept_len.device) if with_alpha else None
+    rc = lib.spec_adapt_k(_ptr(accept_len), _ptr(k_used), _ptr(succ), _ptr(fail), float(decay),
+                          float(c), int(k_min), int(k_max), _ptr(k_next), _ptr(alpha),
+                          _stream_handle(stream), B)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_adapt_k")
+    return k_next, alpha
 
 
 _lm_ws = {}

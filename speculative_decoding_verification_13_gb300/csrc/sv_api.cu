@@ -299,6 +299,20 @@ int spec_lmhead_stats(const void* hidden, const void* unembed, int32_t rows, int
                              static_cast<cudaStream_t>(stream));
 }
 
+int spec_adapt_k(const int32_t* accept_len, const int32_t* k_used, double* succ, double* fail,
+                 double decay, double c, int32_t k_min, int32_t k_max, int32_t* k_next,
+                 float* alpha, void* stream, int32_t batch) {
+  if (batch < 0 || k_min < 0 || k_max < k_min || k_max > SV_MAX_K || !(decay >= 0.0) ||
+      !(decay <= 1.0) || !(c >= 0.0))
+    return SV_ERR_ARG;
+  if (batch == 0) return SV_OK;
+  if (!accept_len || !k_used || !succ || !fail || !k_next) return SV_ERR_ARG;
+  return launch_adapt_k(accept_len, k_used, succ, fail, decay, c, k_min, k_max, k_next, alpha,
+                        batch, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
 int spec_verify_get_error(const void* workspace, void* stream, int32_t* code, int32_t* request,
                           int64_t* row) {
   if (!workspace || !code) return SV_ERR_ARG;

@@ -174,6 +174,9 @@ cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
 size_t kv_workspace_bytes(int32_t B);
 size_t lmhead_workspace_bytes(int M, int V);
+cudaError_t launch_adapt_k(const int32_t* accept_len, const int32_t* k_used, double* succ,
+                           double* fail, double decay, double c, int k_min, int k_max,
+                           int32_t* k_next, float* alpha, int B, cudaStream_t s);
 int launch_lmhead_stats(const void* H, const void* W, int M, int V, int K,
                         const float* temperature, const int32_t* tokens, float* out_m,
                         double* out_s, int32_t* out_arg, float* out_xt, void* workspace,
