@@ -266,15 +266,20 @@ union WarpScratch {
 // bins) and are then ordered within the bin; the bin holding the K-th largest
 // contributes its largest keys after them.
 __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, WarpSel& ws,
-                                          const uint64_t* raw, uint32_t skip) {
+                                          const uint64_t* raw, uint32_t skip, uint32_t lo,
+                                          uint32_t hi) {
   const int lane = threadIdx.x & 31;
   const uint32_t lt = (1u << lane) - 1u;
-  uint32_t lo = ~0u, hi = 0u;
+  // lo / hi: this lane's smallest and largest high key words over the keys
+  // e = lane (mod 32) when the caller has seen them all; ~0u / 0u asks for the
+  // pass below (which also yields ~0u / 0u for a lane that has no key)
+  if (lo == ~0u && hi == 0u) {
 #pragma unroll 4
-  for (int e = lane; e < n; e += 32) {
-    const uint32_t h = uint32_t(keys[e] >> 32);
-    lo = min(lo, h);
-    hi = max(hi, h);
+    for (int e = lane; e < n; e += 32) {
+      const uint32_t h = uint32_t(keys[e] >> 32);
+      lo = min(lo, h);
+      hi = max(hi, h);
+    }
   }
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
@@ -363,7 +368,7 @@ __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, Wa
   }
   big = __any_sync(kFull, big);
   __syncwarp();
-#pragma unroll 2
+#pragma unroll 4
   for (int e = lane; e < n; e += 32) {
     const uint64_t k = keys[e];
     const int bk = bin(k);
@@ -437,14 +442,25 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   for (int r = 0; r < 8; ++r) pre[r] = __ldcg(raw + r * 32 + lane);
   const int n = min(max(w.stats[row].kept, 0), kRawCap);
   const int nc = min(n, kKeyCopy);
+  uint32_t lo = ~0u, hi = 0u;  // the range of the keys, seen as they are copied
 #pragma unroll
   for (int r = 0; r < 8; ++r)
-    if (r * 32 + lane < nc) ws.keys[r * 32 + lane] = pre[r];
+    if (r * 32 + lane < nc) {
+      ws.keys[r * 32 + lane] = pre[r];
+      lo = min(lo, uint32_t(pre[r] >> 32));
+      hi = max(hi, uint32_t(pre[r] >> 32));
+    }
 #pragma unroll 4
-  for (int e = 256 + lane; e < nc; e += 32) ws.keys[e] = __ldcg(raw + e);
+  for (int e = 256 + lane; e < nc; e += 32) {
+    const uint64_t k = __ldcg(raw + e);
+    ws.keys[e] = k;
+    lo = min(lo, uint32_t(k >> 32));
+    hi = max(hi, uint32_t(k >> 32));
+  }
   __syncwarp();
+  if (n > kKeyCopy) lo = ~0u, hi = 0u;  // keys past the copy: select reads them all
   const int nsel = select_sorted(n <= kKeyCopy ? ws.keys : raw, n, K, ws, raw,
-                                 BF16 ? kSkipBf16 : kSkipF32);
+                                 BF16 ? kSkipBf16 : kSkipF32, lo, hi);
 
   const float v0 = composite_value(ws.list[0]);
   // log2(e) / T split into two floats, formed once per row (the FP64 pipe is
@@ -783,6 +799,7 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
     idx[s] = j < Kt ? composite_index(t.list[j]) : INT_MAX;
     p[s] = j < Kt ? t.pk[j] : 0.f;
   }
+#pragma unroll 4
   for (int i = 0; i < Kd; ++i) {
     const int di = composite_index(d->list[i]);
     const float dq = d->pk[i];
@@ -803,6 +820,7 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
     }
     __syncwarp();
     unsigned long long C[2] = {0ull, 0ull}, rmine[2] = {0ull, 0ull};
+#pragma unroll 4
     for (int i = 0; i < Kt; ++i) {
       const int ii = sidx[i];
       const unsigned long long ri = sr[i];
