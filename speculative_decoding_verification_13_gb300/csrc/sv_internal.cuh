@@ -41,7 +41,8 @@ struct WsHeader {
   int32_t n_decide;     // other requests listed by the setup kernel
   int32_t n_draw;       // requests queued for the unfiltered draw
   int32_t next_row;     // draft sampler: rows handed out to warps so far
-  int32_t pad[6];
+  int32_t rp_next;      // row pass: rows claimed past each CTA's first
+  int32_t pad[5];
 };
 
 struct RowStat {

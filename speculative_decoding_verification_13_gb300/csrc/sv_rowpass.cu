@@ -1,7 +1,10 @@
 // Row pass: the one kernel that streams every logit row from HBM once.
 //
-// Persistent, two CTAs per SM.  Warp 0 is the producer: one lane walks the
-// CTA's share of the active-row list and issues TMA bulk copies
+// Persistent, two CTAs per SM.  Warp 0 is the producer: one lane claims rows of
+// the active-row list (its CTA's index first, then the next unclaimed row
+// from a counter, claimed a few tiles before the current row's last copy, so
+// that CTAs streaming faster take more rows and all finish together) and
+// issues TMA bulk copies
 // (cp.async.bulk, 16 KB each) into a 4-stage shared-memory ring, each stage
 // guarded by a "full" mbarrier (transaction bytes) and an "empty" mbarrier (one
 // arrival per consumer warp).  Warps 1..8 consume the tiles and reduce each row
@@ -43,6 +46,7 @@ static_assert(kRowpassCtasPerSm * (kSmemBytes + 4096 + 1024) <= 228 * 1024,
               "shared memory budget for the resident CTAs of one SM");
 
 struct RowShared {
+  RowJob rowq[kStages];  // the row each ring phase starts (row = -1: no more rows)
   int hist[256];
   SelShared sel;
   unsigned long long thmin[3];
@@ -225,30 +229,50 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     long long issued = 0;
     const uint64_t stream_pol = l2_evict_first_policy();
     bool stop = false;
-    for (int j = blockIdx.x; j < n_active && !stop; j += gridDim.x) {
-      const int64_t row = w.rowlist[j].row;
+    // Each row's first ring phase carries its entry in S.rowq (the consumers
+    // read it once the phase completes); a row without bulk tiles, and the
+    // end of the list, take a phase of their own with no copy.  `issued`
+    // counts phases.
+    const int claim_t = ntiles > 4 ? ntiles - 4 : 0;
+    int j = blockIdx.x;
+    RowJob job = w.rowlist[min(j, max(n_active - 1, 0))];
+    for (uint32_t q = 0; !stop; ++q) {
+      const bool end = j >= n_active;
+      if (end) job.row = -1;
+      const int64_t row = job.row;
       const char* src =
           row < P.Rt
               ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
               : static_cast<const char*>(P.draft) + (row - P.Rt) * P.d_stride * E::kSize;
-      for (int t = 0; t < ntiles; ++t) {
-        const int64_t rem = bulk - int64_t(t) * kTileBytes;
-        const uint32_t bytes = uint32_t(rem < kTileBytes ? rem : kTileBytes);
+      const int nt = end ? 0 : ntiles;
+      int jn = n_active;
+      for (int t = 0; t < (nt > 0 ? nt : 1); ++t) {
         if (!wait_or_abort(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
           *reinterpret_cast<volatile int*>(&S.pabort) = 1;
           record_error(w.hdr, SV_ERR_TIMEOUT, -1, row);
           stop = true;
           break;
         }
-        mbar_arrive_expect_tx(full0 + 8u * stage, bytes);
-        bulk_load_hint(smem_addr(ring + size_t(stage) * kTileBytes), src + int64_t(t) * kTileBytes,
-                       bytes, full0 + 8u * stage, stream_pol);
+        if (t == 0) S.rowq[q % kStages] = job;
+        if (t == claim_t && !end) jn = int(gridDim.x) + atomicAdd(&w.hdr->rp_next, 1);
+        if (nt == 0) {
+          mbar_arrive(full0 + 8u * stage);
+        } else {
+          const int64_t rem = bulk - int64_t(t) * kTileBytes;
+          const uint32_t bytes = uint32_t(rem < kTileBytes ? rem : kTileBytes);
+          mbar_arrive_expect_tx(full0 + 8u * stage, bytes);
+          bulk_load_hint(smem_addr(ring + size_t(stage) * kTileBytes),
+                         src + int64_t(t) * kTileBytes, bytes, full0 + 8u * stage, stream_pol);
+        }
         ++issued;
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (end) break;
+      j = jn;
+      if (j < n_active) job = w.rowlist[j];
     }
     if (stop || *reinterpret_cast<volatile int*>(&S.cabort)) {
       // Let every copy this CTA issued land before the CTA may exit.
@@ -292,21 +316,24 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
   };
   unsigned bad_seen = 0u;  // value of S.nbad after the previous row
 
-  // The next row's entry is loaded one row ahead, one 32-bit field per lane
-  // (lanes 0..5), and broadcast when its row starts.
-  auto load_entry = [&](int j) -> int {
-    return lane < 6 && j < n_active ? reinterpret_cast<const int*>(w.rowlist + j)[lane] : 0;
-  };
-  int nxt = load_entry(blockIdx.x);
-  for (int j = blockIdx.x; j < n_active; j += gridDim.x) {
-    const int cur = nxt;
-    nxt = load_entry(j + gridDim.x);
-    const int64_t row = __shfl_sync(0xffffffffu, cur, 0);
-    const int b = __shfl_sync(0xffffffffu, cur, 1);
-    const int gx = __shfl_sync(0xffffffffu, cur, 2);
-    const int mode = __shfl_sync(0xffffffffu, cur, 3) & 3;
-    const float T = __int_as_float(__shfl_sync(0xffffffffu, cur, 4));
-    const int Kreq = __shfl_sync(0xffffffffu, cur, 5);
+  for (uint32_t q = 0;; ++q) {
+    // The row's first phase holds its entry.  A wait that fails sets
+    // S.cabort before the first barrier, and no thread can set it again
+    // before the second, so all threads take the same branch.
+    acquire();
+    consumer_sync();
+    const int ab0 = *reinterpret_cast<volatile int*>(&S.cabort);
+    consumer_sync();
+    if (ab0) break;
+    const RowJob ent = S.rowq[q % kStages];
+    if (ent.row < 0) break;  // no more rows
+    if (ntiles == 0) release();  // a phase without a copy
+    const int64_t row = ent.row;
+    const int b = ent.b;
+    const int gx = ent.gx;
+    const int mode = ent.mode & 3;
+    const float T = ent.T;
+    const int Kreq = ent.K;
     const void* rowp =
         row < P.Rt ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
                    : static_cast<const char*>(P.draft) + (row - P.Rt) * P.d_stride * E::kSize;

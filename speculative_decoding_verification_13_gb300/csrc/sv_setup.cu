@@ -9,6 +9,7 @@ namespace sv {
 namespace {
 
 constexpr int kSetupThreads = 1024;
+constexpr int kSetupCtas = 8;  // CTAs that share the row-list writes
 
 // Exclusive scan over the CTA; *total receives the sum.  Two counters travel
 // packed in one 64-bit word (each field's sum over a chunk stays below 2^32).
@@ -43,19 +44,75 @@ __device__ __forceinline__ unsigned long long pack2(uint32_t lo, uint32_t hi) {
   return (static_cast<unsigned long long>(hi) << 32) | lo;
 }
 
+// One request of the current chunk, as the row-list fill needs it.
+struct ReqRows {
+  int a0;      // first entry of the request in the row list
+  int t0, d0;  // first target row, first draft row (relative to R_t)
+  int k;       // drafts
+  int active;  // entries: k + 1 target rows, then the k draft rows when streamed
+  int modes;   // target row mode | draft row mode << 8 | 1 << 16 when the
+               // draft rows are not streamed (they get a defined record here)
+  int tk;      // top-k
+  float T;     // temperature
+};
+
+// Writes the row list of the chunk's requests, one warp per request, so that
+// consecutive lanes write consecutive 32-byte entries (a thread walking its
+// own request's entries would leave every store uncoalesced).  The requests
+// are spread over the warps of every CTA of the grid: the list is a few
+// hundred KB, more than one SM writes out quickly.
+__device__ void fill_rows(const Problem& P, const ReqRows* rq, int base, int nb) {
+  const Ws& w = P.ws;
+  const int lane = threadIdx.x & 31;
+  constexpr int kW = kSetupThreads / 32;
+  for (int r = blockIdx.x * kW + (threadIdx.x >> 5); r < nb; r += gridDim.x * kW) {
+    const ReqRows q = rq[r];
+    for (int e = lane; e < q.active; e += 32) {
+      const bool tgt = e <= q.k;
+      const int i = tgt ? e : e - q.k - 1;
+      const int row = tgt ? q.t0 + i : int(P.Rt) + q.d0 + i;
+      const int gx = i < q.k ? P.draft_tokens[q.d0 + i] : -1;
+      const int mode = (i << 2) | (tgt ? (q.modes & 0xff) : ((q.modes >> 8) & 0xff));
+      int4* dst = reinterpret_cast<int4*>(w.rowlist + q.a0 + e);
+      dst[0] = make_int4(row, base + r, gx, mode);
+      dst[1] = make_int4(__float_as_int(q.T), q.tk, 0, 0);
+    }
+    if (q.modes >> 16)
+      // Rows the streaming pass will not visit still get a defined record.
+      for (int i = lane; i < q.k; i += 32) {
+        RowStat st;
+        st.s = 0.0;
+        st.pg = __longlong_as_double(0x7ff8000000000000LL);
+        st.m = 0.0f;
+        st.arg = -1;
+        st.kept = 0;
+        st.mode = kSkip;
+        w.stats[P.Rt + q.d0 + i] = st;
+      }
+  }
+}
+
 __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   const Ws& w = P.ws;
   __shared__ int s_bad;
+  __shared__ ReqRows s_req[kSetupThreads];
   pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
+  // Every CTA forms the same offsets, modes and scans; CTA 0 alone writes the
+  // header, the offsets, the flags and the job lists, and each CTA writes its
+  // share of the row list.  (More than one CTA only when B <= kSetupThreads.)
+  const bool lead = blockIdx.x == 0;
   if (threadIdx.x == 0) {
-    w.hdr->err_code = 0;
-    w.hdr->err_req = -1;
-    w.hdr->err_row = -1;
-    w.hdr->n_active = 0;
-    w.hdr->global_err = 0;
-    w.hdr->n_filtered = 0;
-    w.hdr->n_decide = 0;
-    w.hdr->n_draw = 0;
+    if (lead) {
+      w.hdr->err_code = 0;
+      w.hdr->err_req = -1;
+      w.hdr->err_row = -1;
+      w.hdr->n_active = 0;
+      w.hdr->global_err = 0;
+      w.hdr->n_filtered = 0;
+      w.hdr->n_decide = 0;
+      w.hdr->n_draw = 0;
+      w.hdr->rp_next = 0;
+    }
     s_bad = 0;
   }
   __syncthreads();
@@ -78,7 +135,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
         tk1 = P.top_k ? P.top_k[b] : 0;
       }
       if (k < 0 || k > SV_MAX_K) {
-        record_error(w.hdr, SV_ERR_DATA_K, b, -1);
+        if (lead) record_error(w.hdr, SV_ERR_DATA_K, b, -1);
         atomicOr(&s_bad, 1);
         k = 0;
       }
@@ -86,19 +143,21 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     unsigned long long tot;
     const unsigned long long ex =
         block_exclusive_scan(b < P.B ? pack2(uint32_t(k + 1), uint32_t(k)) : 0ull, &tot);
-    if (b < P.B) w.t_off[b] = carry + int(uint32_t(ex));
+    if (b < P.B && lead) w.t_off[b] = carry + int(uint32_t(ex));
     k1 = k;
     t01 = carry + int(uint32_t(ex));
     carry += int(uint32_t(tot));
     carry_d += int(uint32_t(tot >> 32));
   }
   if (threadIdx.x == 0) {
-    w.t_off[P.B] = carry;
     if (!s_bad && (carry != P.Rt || carry_d != P.Rd)) {
-      record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
+      if (lead) record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
       s_bad = 1;
     }
-    if (s_bad) w.hdr->global_err = 1;
+    if (lead) {
+      w.t_off[P.B] = carry;
+      if (s_bad) w.hdr->global_err = 1;
+    }
   }
   __syncthreads();
   if (s_bad) return;
@@ -135,13 +194,14 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
         }
         if (bad) code = SV_ERR_DATA_TOKEN;
       }
-      w.req_flag[b] = code;
-      if (code) {
-        record_error(w.hdr, code, b, -1);
-      } else if (T == 0.0f) {
+      if (lead) {
+        w.req_flag[b] = code;
+        if (code) record_error(w.hdr, code, b, -1);
+      }
+      if (code == 0 && T == 0.0f) {
         mode_t = kArgmax;
         active = k + 1;
-      } else {
+      } else if (code == 0) {
         mode_t = mode_d = filtered ? kTopk : kStats;
         active = 2 * k + 1;
       }
@@ -158,41 +218,41 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     carry_a += int(uint32_t(tot));
     carry_f += int((tot >> 32) & 0xffffu);
     carry_o += int(tot >> 48);
-    if (b < P.B) {
+    if (b < P.B && lead) {
       w.seg_cnt[b] = 0;
       if (filt)
         w.job[f0] = make_int4(b, 0, t0, k);
       else
         w.job[P.B + o0] = make_int4(b, 0, t0, k);
     }
-    if (b < P.B && active) {
-      int a = a0;
-      for (int i = 0; i <= k; ++i) {
-        const int gx = i < k ? P.draft_tokens[d0 + i] : -1;
-        w.rowlist[a++] = RowJob{t0 + i, b, gx, (i << 2) | mode_t, T, tk, {0, 0}};
-      }
-      if (mode_d != kSkip)
-        for (int i = 0; i < k; ++i)
-          w.rowlist[a++] = RowJob{(int)P.Rt + d0 + i, b, P.draft_tokens[d0 + i],
-                                  (i << 2) | mode_d, T, tk, {0, 0}};
-    }
-    if (b < P.B && (code || mode_d == kSkip)) {
-      // Rows the streaming pass will not visit still get a defined record.
-      for (int i = 0; i < k; ++i) {
-        RowStat& st = w.stats[P.Rt + d0 + i];
-        st.s = 0.0;
-        st.pg = __longlong_as_double(0x7ff8000000000000LL);
-        st.m = 0.0f;
-        st.arg = -1;
-        st.kept = 0;
-        st.mode = kSkip;
-      }
-    }
+    s_req[threadIdx.x] =
+        ReqRows{a0, t0, d0, k, b < P.B ? active : 0,
+                mode_t | (mode_d << 8) | (b < P.B && mode_d == kSkip ? 1 << 16 : 0), tk, T};
+    __syncthreads();
+    fill_rows(P, s_req, base, min(kSetupThreads, P.B - base));
+    __syncthreads();  // s_req is rewritten by the next chunk
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && lead) {
     w.hdr->n_active = carry_a;
     w.hdr->n_filtered = carry_f;
     w.hdr->n_decide = carry_o;
+  }
+}
+
+// The draft sampler's row list, one warp per request (coalesced entries):
+// request b's drafter rows d_off[b] + i, i < k_b, all in the request's mode,
+// reporting no token.
+__device__ void fill_sample_rows(const Problem& P, const ReqRows* rq, int base, int nb) {
+  const Ws& w = P.ws;
+  const int lane = threadIdx.x & 31;
+  constexpr int kW = kSetupThreads / 32;
+  for (int r = blockIdx.x * kW + (threadIdx.x >> 5); r < nb; r += gridDim.x * kW) {
+    const ReqRows q = rq[r];
+    for (int i = lane; i < q.active; i += 32) {
+      int4* dst = reinterpret_cast<int4*>(w.rowlist + q.a0 + i);
+      dst[0] = make_int4(q.t0 + i, base + r, -1, (i << 2) | q.modes);
+      dst[1] = make_int4(__float_as_int(q.T), q.tk, 0, 0);
+    }
   }
 }
 
@@ -205,8 +265,13 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
 __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Problem P) {
   const Ws& w = P.ws;
   __shared__ int s_bad;
+  __shared__ ReqRows s_req[kSetupThreads];
   pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
-  if (threadIdx.x == 0) {
+  // As in the verifier's setup: CTA 0 writes the header, offsets, flags and
+  // the outputs of failed requests; every CTA writes its share of the row
+  // list and of the zeroed counters.
+  const bool lead = blockIdx.x == 0;
+  if (threadIdx.x == 0 && lead) {
     w.hdr->err_code = 0;
     w.hdr->err_req = -1;
     w.hdr->err_row = -1;
@@ -216,13 +281,19 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     w.hdr->n_decide = 0;
     w.hdr->n_draw = 0;
     w.hdr->next_row = 0;
-    s_bad = 0;
+    w.hdr->rp_next = 0;
   }
+  if (threadIdx.x == 0) s_bad = 0;
   // every row may queue a draw: their segment counters start at zero
-  for (int64_t q = threadIdx.x; q < P.Rt; q += kSetupThreads) w.seg_cnt[q] = 0;
+  for (int64_t q = int64_t(blockIdx.x) * kSetupThreads + threadIdx.x; q < P.Rt;
+       q += int64_t(gridDim.x) * kSetupThreads)
+    w.seg_cnt[q] = 0;
   __syncthreads();
 
   // Pass 1: row offsets; a k outside [0, SV_MAX_K] makes the layout undefined.
+  // With a single chunk (B <= kSetupThreads) each offset stays in a register.
+  const bool one = P.B <= kSetupThreads;
+  int d01 = 0;
   int carry = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
@@ -230,23 +301,26 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     if (b < P.B) {
       k = P.k_per_req[b];
       if (k < 0 || k > SV_MAX_K) {
-        record_error(w.hdr, SV_ERR_DATA_K, b, -1);
+        if (lead) record_error(w.hdr, SV_ERR_DATA_K, b, -1);
         atomicOr(&s_bad, 1);
         k = 0;
       }
     }
     unsigned long long tot;
     const unsigned long long ex = block_exclusive_scan(b < P.B ? pack2(uint32_t(k), 0u) : 0ull, &tot);
-    if (b < P.B) w.t_off[b] = carry + int(uint32_t(ex));
+    if (b < P.B && lead) w.t_off[b] = carry + int(uint32_t(ex));
+    d01 = carry + int(uint32_t(ex));
     carry += int(uint32_t(tot));
   }
   if (threadIdx.x == 0) {
-    w.t_off[P.B] = carry;
     if (!s_bad && carry != P.Rt) {
-      record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
+      if (lead) record_error(w.hdr, SV_ERR_DATA_ROWS, -1, -1);
       s_bad = 1;
     }
-    if (s_bad) w.hdr->global_err = 1;
+    if (lead) {
+      w.t_off[P.B] = carry;
+      if (s_bad) w.hdr->global_err = 1;
+    }
   }
   __syncthreads();
   if (s_bad) return;
@@ -259,7 +333,7 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     float T = 0.f;
     if (b < P.B) {
       k = P.k_per_req[b];
-      d0 = w.t_off[b];
+      d0 = one ? d01 : w.t_off[b];
       T = P.temperature[b];
       const float tp = P.top_p ? P.top_p[b] : 1.0f;
       tk = P.top_k ? P.top_k[b] : 0;
@@ -269,14 +343,17 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
       else if (!(tp > 0.0f && tp <= 1.0f)) code = SV_ERR_DATA_TOP_P;
       else if (tk < 0) code = SV_ERR_DATA_TOP_K;
       else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
-      w.req_flag[b] = code;
-      if (code) {
+      if (code && lead) {
+        w.req_flag[b] = code;
         record_error(w.hdr, code, b, -1);
         for (int i = 0; i < k; ++i) {
           P.out_tokens[d0 + i] = -1;
           if (P.out_q) P.out_q[d0 + i] = __int_as_float(0x7fc00000);
         }
-      } else {
+      } else if (lead) {
+        w.req_flag[b] = 0;
+      }
+      if (!code) {
         mode = T == 0.0f ? kArgmax : (filtered ? kTopk : kStats);
         active = k;
       }
@@ -284,21 +361,28 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     unsigned long long tot;
     const int a0 = carry_a + int(uint32_t(block_exclusive_scan(uint32_t(active), &tot)));
     carry_a += int(uint32_t(tot));
-    for (int i = 0; i < active; ++i)
-      w.rowlist[a0 + i] = RowJob{d0 + i, b, -1, (i << 2) | mode, T, tk, {0, 0}};
+    // fill_sample_rows reads a0, t0 (the first drafter row), active, modes, tk, T
+    s_req[threadIdx.x] = ReqRows{a0, d0, 0, k, active, mode, tk, T};
+    __syncthreads();
+    fill_sample_rows(P, s_req, base, min(kSetupThreads, P.B - base));
+    __syncthreads();  // s_req is rewritten by the next chunk
   }
-  if (threadIdx.x == 0) w.hdr->n_active = carry_a;
+  if (threadIdx.x == 0 && lead) w.hdr->n_active = carry_a;
 }
 
 }  // namespace
 
+// More than one CTA only with a single chunk of requests: the CTAs other than
+// the first rely on the offsets they keep in registers.
+int setup_grid(int64_t B) { return B <= kSetupThreads ? kSetupCtas : 1; }
+
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s) {
-  sample_setup_kernel<<<1, kSetupThreads, 0, s>>>(P);
+  sample_setup_kernel<<<setup_grid(P.B), kSetupThreads, 0, s>>>(P);
   return cudaGetLastError();
 }
 
 cudaError_t launch_setup(const Problem& P, cudaStream_t s) {
-  setup_kernel<<<1, kSetupThreads, 0, s>>>(P);
+  setup_kernel<<<setup_grid(P.B), kSetupThreads, 0, s>>>(P);
   return cudaGetLastError();
 }
 
