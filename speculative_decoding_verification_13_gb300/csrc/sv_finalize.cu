@@ -224,6 +224,7 @@ constexpr int kKeyCopy = 512;  // survivors copied to shared memory (more are re
 constexpr int kBinSort = 8;    // whole bins up to this size are ordered by insertion sort
 constexpr int kFastDraw = 64;  // kept sets up to this size are drawn from shared memory
 constexpr int kRankMax = 64;   // boundary bins up to this size are ordered by ranks
+constexpr int kRankAll = 128;  // candidate sets up to this size are ordered by ranks
 
 // Per-warp scratch of one filtered row.  After the row it still holds the
 // row's kept set (sorted keys and probabilities) and p(x) of its token, which
@@ -261,10 +262,12 @@ union WarpScratch {
 // The min(n, K) largest of the n unique survivor keys at keys[] (shared or
 // global memory), sorted descending into ws.list; returns their count.  One
 // pass bins the keys into 256 ordered bins linear in the logit over [min,
-// max] (a monotone map, so a higher bin holds only larger keys).  Bins wholly
-// inside the top K go straight to their final slots (a counting sort over
-// bins) and are then ordered within the bin; the bin holding the K-th largest
-// contributes its largest keys after them.
+// max] (a monotone map, so a higher bin holds only larger keys) and finds the
+// bin holding the K-th largest.  When few keys lie in that bin or above, each
+// takes its rank among them as its slot; otherwise bins wholly inside the top
+// K go straight to their final slots (a counting sort over bins) and are then
+// ordered within the bin, and the boundary bin contributes its largest keys
+// after them.  ws.keys may be overwritten.
 __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, WarpSel& ws,
                                           const uint64_t* raw, uint32_t skip, uint32_t lo,
                                           uint32_t hi) {
@@ -359,6 +362,40 @@ __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, Wa
     for (int j = nsel + lane; j < P2; j += 32) ws.list[j] = 0ull;
     __syncwarp();
     sort_desc(ws.list, P2);
+    return nsel;
+  }
+  const int ns = bm ? above + gcnt : n;  // keys in the boundary bin or above
+  if (ns <= kRankAll) {
+    // Few candidates (the usual case for a small k): compact the keys of the
+    // bins at or above the boundary into ws.keys (in place when they are
+    // there: a key only moves down), then each key's slot is its rank among
+    // them, the number of larger keys (keys are unique).
+    int c = 0;
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int e = e0 + lane;
+      const uint64_t k = e < n ? keys[e] : 0ull;
+      const bool in = e < n && bin(k) >= bstar;
+      const uint32_t bal = __ballot_sync(kFull, in);
+      __syncwarp();  // every lane has read its key before any lane writes
+      if (in) ws.keys[c + __popc(bal & lt)] = k;
+      c += __popc(bal);
+    }
+    __syncwarp();
+    for (int e0 = 0; e0 < ns; e0 += 64) {
+      const int ea = e0 + lane, eb = ea + 32;
+      const uint64_t a = ea < ns ? ws.keys[ea] : ~0ull;
+      const uint64_t b = eb < ns ? ws.keys[eb] : ~0ull;
+      int ra = 0, rb = 0;
+#pragma unroll 8
+      for (int t = 0; t < ns; ++t) {
+        const uint64_t x = ws.keys[t];
+        ra += x > a;
+        rb += x > b;
+      }
+      if (ea < ns && ra < nsel) ws.list[ra] = a;
+      if (eb < ns && rb < nsel) ws.list[rb] = b;
+    }
+    __syncwarp();
     return nsel;
   }
 #pragma unroll
