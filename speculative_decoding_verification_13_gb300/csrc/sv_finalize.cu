@@ -301,8 +301,14 @@ __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, Wa
   for (int j = 0; j < 8; ++j) ws.hw[lane * 8 + j] = 0;
   if (lane == 0) ws.gcount = 0;
   __syncwarp();
+  // each key's bin is kept (one byte, in ws.grp) for the compaction below
+  uint8_t* kbin = reinterpret_cast<uint8_t*>(ws.grp);
 #pragma unroll 4
-  for (int e = lane; e < n; e += 32) atomicAdd(&ws.hw[bin(keys[e])], 1);
+  for (int e = lane; e < n; e += 32) {
+    const int bk = bin(keys[e]);
+    kbin[e] = uint8_t(bk);
+    atomicAdd(&ws.hw[bk], 1);
+  }
   __syncwarp();
   // lane holds bins 8 lane .. 8 lane + 7; off[j]: keys in the bins above
   int cnt[8], off[8], loc = 0;
@@ -371,14 +377,15 @@ __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, Wa
     // there: a key only moves down), then each key's slot is its rank among
     // them, the number of larger keys (keys are unique).
     int c = 0;
-    for (int e0 = 0; e0 < n; e0 += 32) {
-      const int e = e0 + lane;
-      const uint64_t k = e < n ? keys[e] : 0ull;
-      const bool in = e < n && bin(k) >= bstar;
-      const uint32_t bal = __ballot_sync(kFull, in);
-      __syncwarp();  // every lane has read its key before any lane writes
-      if (in) ws.keys[c + __popc(bal & lt)] = k;
-      c += __popc(bal);
+    for (int e0 = 0; e0 < n; e0 += 64) {
+      const int ea = e0 + lane, eb = ea + 32;
+      const uint64_t ka = ea < n ? keys[ea] : 0ull, kb = eb < n ? keys[eb] : 0ull;
+      const bool ia = ea < n && int(kbin[ea]) >= bstar, ib = eb < n && int(kbin[eb]) >= bstar;
+      const uint32_t ba = __ballot_sync(kFull, ia), bb = __ballot_sync(kFull, ib);
+      __syncwarp();  // every lane has read its keys before any lane writes
+      if (ia) ws.keys[c + __popc(ba & lt)] = ka;
+      if (ib) ws.keys[c + __popc(ba) + __popc(bb & lt)] = kb;
+      c += __popc(ba) + __popc(bb);
     }
     __syncwarp();
     for (int e0 = 0; e0 < ns; e0 += 64) {
@@ -466,9 +473,23 @@ __device__ __noinline__ int select_sorted(const uint64_t* keys, int n, int K, Wa
 // set in ws.  Weights are float-accurate (relative error a few 1e-7) with
 // exact fixed-point prefix sums; a top-p cut within 2^-17 of the threshold is
 // redone in double precision, so the kept set is the double-precision one.
+// log2(e) / T as the unevaluated sum chi + clo of two floats, formed in double
+// by lane 0 (the FP64 pipe is narrow: per-lane double work would queue on it)
+// and broadcast to the warp.
+__device__ __forceinline__ void log2e_over_t(float T, float* chi, float* clo) {
+  float h = 0.f, l = 0.f;
+  if ((threadIdx.x & 31) == 0) {
+    const double cd = 1.4426950408889634 / double(T);
+    h = float(cd);
+    l = float(cd - double(h));
+  }
+  *chi = __shfl_sync(kFull, h, 0);
+  *clo = __shfl_sync(kFull, l, 0);
+}
+
 template <bool BF16>
-__device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float tp, int gx,
-                                WarpSel& ws) {
+__device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float chi,
+                                             float clo, float tp, int gx, WarpSel& ws) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
   const uint64_t* raw = w.cand_raw + size_t(row) * kRawCap;
@@ -500,16 +521,6 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
                                  BF16 ? kSkipBf16 : kSkipF32, lo, hi);
 
   const float v0 = composite_value(ws.list[0]);
-  // log2(e) / T split into two floats, formed once per row (the FP64 pipe is
-  // narrow: per-lane double work would queue on it)
-  float chi = 0.f, clo = 0.f;
-  if (lane == 0) {
-    const double cd = 1.4426950408889634 / double(T);
-    chi = float(cd);
-    clo = float(cd - double(chi));
-  }
-  chi = __shfl_sync(kFull, chi, 0);
-  clo = __shfl_sync(kFull, clo, 0);
   // weights and the fixed-point mass before each j (integer work; the FP64
   // pipe, scarce on this part, is kept for a few operations per row)
   unsigned long long W = 0ull;
@@ -919,6 +930,10 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
   const int K = P.top_k[b];
   const float T = P.temperature[b];
   const float tp = P.top_p ? P.top_p[b] : 1.0f;
+  float chi, clo;  // once per request
+  log2e_over_t(T, &chi, &clo);
+  // the final draw's uniform, fetched while the waves run
+  const float u_last = warp == 0 ? P.uniforms[t0 + k] : 0.f;
   int w0 = 0;
   for (;; w0 += kWave) {
     const int pos = w0 + (warp >> 1);
@@ -926,9 +941,9 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
     if (warp == 0 && lane < kWave && w0 + lane < k) u = P.uniforms[t0 + w0 + lane];
     if (pos < k) {
       const int64_t row = (warp & 1) ? P.Rt + d0 + pos : int64_t(t0) + pos;
-      warp_filter_row<BF16>(P, row, K, T, tp, P.draft_tokens[d0 + pos], scr[warp].sel);
+      warp_filter_row<BF16>(P, row, K, T, chi, clo, tp, P.draft_tokens[d0 + pos], scr[warp].sel);
     } else if (warp == 2 * max(k - w0, 0)) {
-      warp_filter_row<BF16>(P, t0 + k, K, T, tp, -1, scr[warp].sel);
+      warp_filter_row<BF16>(P, t0 + k, K, T, chi, clo, tp, -1, scr[warp].sel);
     }
     __syncthreads();
     if (warp == 0) {
@@ -962,7 +977,7 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
     // was filtered by warp 2 (L - w0), its draft row by the next warp
     const int tw = 2 * (L - w0);
     const bool residual = L < k;
-    const double u = double(P.uniforms[t0 + k]);
+    const double u = double(u_last);
     const WarpSel& ts = scr[tw].sel;
     int y;
     if (ts.fast && (!residual || scr[tw + 1].sel.fast))
@@ -1061,7 +1076,9 @@ __global__ void __launch_bounds__(kPostThreads, 2) sample_post_kernel(const Prob
       y = __ldcg(&w.stats[row].arg);
     } else if (mode == kTopk) {
       const float tp = P.top_p ? P.top_p[job.b] : 1.0f;
-      warp_filter_row<BF16>(P, row, job.K, job.T, tp, -1, ws.sel);
+      float chi, clo;
+      log2e_over_t(job.T, &chi, &clo);
+      warp_filter_row<BF16>(P, row, job.K, job.T, chi, clo, tp, -1, ws.sel);
       if (ws.sel.fast) {
         y = draw_fast(ws.sel, nullptr, u, ws.sel.hw, ws.sel.before, &qy);
       } else {
