@@ -523,23 +523,29 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   const float v0 = composite_value(ws.list[0]);
   // weights and the fixed-point mass before each j (integer work; the FP64
   // pipe, scarce on this part, is kept for a few operations per row)
+  // two consecutive entries per lane, one scan of the pair sums per 64
   unsigned long long W = 0ull;
-  for (int j0 = 0; j0 < nsel; j0 += 32) {
-    const int j = j0 + lane;
-    unsigned long long fx = 0ull;
-    if (j < nsel) {
-      const float v = composite_value(ws.list[j]);
-      float f = 0.f;
-      int e2 = 0;
-      if (v > -INFINITY) {
-        f = weight_split(v, v0, chi, clo, &e2);
-        fx = fix55(f, e2);
+  for (int j0 = 0; j0 < nsel; j0 += 64) {
+    const int j = j0 + 2 * lane;
+    unsigned long long fx[2] = {0ull, 0ull};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (j + h < nsel) {
+        const float v = composite_value(ws.list[j + h]);
+        float f = 0.f;
+        int e2 = 0;
+        if (v > -INFINITY) {
+          f = weight_split(v, v0, chi, clo, &e2);
+          fx[h] = fix55(f, e2);
+        }
+        ws.pk[j + h] = f;
+        ws.hw[j + h] = e2;
       }
-      ws.pk[j] = f;
-      ws.hw[j] = e2;
-    }
-    const unsigned long long incl = warp_incl_scan(fx);
-    if (j < nsel) ws.before[j] = W + incl - fx;
+    const unsigned long long pair = fx[0] + fx[1];
+    const unsigned long long incl = warp_incl_scan(pair);
+    const unsigned long long excl = W + incl - pair;
+    if (j < nsel) ws.before[j] = excl;
+    if (j + 1 < nsel) ws.before[j + 1] = excl + fx[0];
     W += __shfl_sync(kFull, incl, 31);
   }
   __syncwarp();
