@@ -294,6 +294,15 @@ def test_data_errors_are_reported_per_request():
     _expect(b, 22, {0, 1})
 
 
+def test_every_request_failing_validation():
+    """No row is streamed (every request fails the setup kernel's checks): the
+    row pass's CTAs find only the end of the row list."""
+    b = custom([2, 3, 1, 4], [1.0, 1.0, 0.0, 0.7], 500, torch.bfloat16)
+    b.temperature[:] = -1.0
+    g = _expect(b, 17, {0, 1, 2, 3})
+    assert (g["tok"] == -1).all()
+
+
 def test_batch_level_errors():
     b = custom([2, 3], [1.0, 1.0], 300, torch.float32)
     b.k_per_req[0] = 33

@@ -95,6 +95,21 @@ def test_large_kept_sets_take_the_general_draw():
     assert code == 0
 
 
+def test_many_requests_several_setup_chunks():
+    """1500 requests: more than one chunk of the setup kernel (1024 requests),
+    so it runs as one CTA that keeps the row offsets in memory."""
+    rng = np.random.default_rng(41)
+    B = 1500
+    k = rng.integers(0, 5, B).tolist()
+    kind = rng.integers(0, 3, B)
+    T = np.where(kind == 0, 0.0, rng.uniform(0.5, 1.5, B)).tolist()
+    tk = np.where(kind == 2, rng.integers(1, 40, B), 0).tolist()
+    tp = np.where(kind == 2, rng.uniform(0.5, 1.0, B), 1.0).tolist()
+    code, _, _ = check(sample_case("B=1500", k, T, 1000, torch.float32, 41, top_k=tk, top_p=tp),
+                       "B=1500")
+    assert code == 0
+
+
 def test_data_errors_fail_their_requests_only():
     k = [2, 3, 2, 1]
     x, kk, T, tk, tp, u = sample_case("errors", k, [1.0, 1.0, 0.8, 1.0], 500, torch.float32, 36)
