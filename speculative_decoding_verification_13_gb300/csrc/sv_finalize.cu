@@ -251,13 +251,14 @@ struct WarpSel {
   int kp;      // kept size
   int fast;    // pk[0 .. kp) holds the kept probabilities and kp <= kFastDraw
   int gcount;  // keys collected from the boundary bin
-  int pad;
+  int pad[3];
 };
 
 union WarpScratch {
   WarpSel sel;
   DrawScratch draw;
 };
+static_assert(sizeof(WarpScratch) % 16 == 0, "keys of every warp's scratch are 16-byte aligned");
 
 // The min(n, K) largest of the n unique survivor keys at keys[] (shared or
 // global memory), sorted descending into ws.list; returns their count.  One
@@ -487,20 +488,27 @@ __device__ __forceinline__ void log2e_over_t(float T, float* chi, float* clo) {
   *clo = __shfl_sync(kFull, l, 0);
 }
 
+// n_pre >= 0: the first kKeyCopy survivor slots are already in ws.keys
+// (copied ahead, see filtered_request) and n_pre is the survivor count.
 template <bool BF16>
 __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int K, float T, float chi,
-                                             float clo, float tp, int gx, WarpSel& ws) {
+                                             float clo, float tp, int gx, WarpSel& ws,
+                                             int n_pre = -1) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
   const uint64_t* raw = w.cand_raw + size_t(row) * kRawCap;
+  int n;
+  uint32_t lo = ~0u, hi = 0u;  // the range of the keys, seen as they are copied
+  if (n_pre >= 0) {
+    n = min(n_pre, kRawCap);  // the range is taken by select_sorted
+  } else {
   // the first 256 key slots are fetched together with the survivor count
   // (the row's kRawCap slots are all addressable)
   uint64_t pre[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) pre[r] = __ldcg(raw + r * 32 + lane);
-  const int n = min(max(w.stats[row].kept, 0), kRawCap);
+  n = min(max(w.stats[row].kept, 0), kRawCap);
   const int nc = min(n, kKeyCopy);
-  uint32_t lo = ~0u, hi = 0u;  // the range of the keys, seen as they are copied
 #pragma unroll
   for (int r = 0; r < 8; ++r)
     if (r * 32 + lane < nc) {
@@ -517,6 +525,7 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   }
   __syncwarp();
   if (n > kKeyCopy) lo = ~0u, hi = 0u;  // keys past the copy: select reads them all
+  }
   const int nsel = select_sorted(n <= kKeyCopy ? ws.keys : raw, n, K, ws, raw,
                                  BF16 ? kSkipBf16 : kSkipF32, lo, hi);
 
@@ -918,6 +927,41 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
   return -1;  // not reached: the second attempt always returns
 }
 
+// The row that wave slot s (a warp index: position w0 + s / 2, target row
+// for even s, draft row for odd s) of a filtered request filters, or -1; the
+// bonus row k goes to the first slot left after position k - 1 (slot 0 of
+// one more wave when k is a multiple of kWave).  *gx: the token whose
+// probability the row reports.
+__device__ __forceinline__ int64_t wave_row(const Problem& P, int b, int t0, int k, int w0, int s,
+                                            int* gx) {
+  const int d0 = t0 - b, pos = w0 + (s >> 1);
+  if (pos < k) {
+    *gx = P.draft_tokens[d0 + pos];
+    return (s & 1) ? P.Rt + d0 + pos : int64_t(t0) + pos;
+  }
+  *gx = -1;
+  return s == 2 * (k - w0) ? int64_t(t0) + k : -1;
+}
+
+// Asynchronous copy of the first kKeyCopy survivor slots of a row into a
+// warp's scratch (16 bytes per lane per step, through L2 only).
+__device__ __forceinline__ void copy_keys_async(const uint64_t* raw, uint64_t* keys) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < kKeyCopy / 64; ++i) {
+    const int c = i * 32 + lane;  // 16-byte chunk: keys 2c, 2c + 1
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(keys + 2 * c)),
+                 "l"(raw + 2 * c)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void copy_keys_wait() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncwarp();
+}
+
 // A filtered request, by one CTA, in waves of kWave positions: warps 2j and
 // 2j + 1 filter the target and draft rows of position w0 + j, the first spare
 // warp of the wave that reaches position k - 1 filters the bonus row k (when
@@ -927,7 +971,10 @@ __device__ __noinline__ int draw_fast(const WarpSel& t, const WarpSel* d, double
 // rejection, so rows past it are never filtered.  (p, q) are reported for the
 // positions up to the stop, NaN after it.  The final draw reads the kept sets
 // of the stopping position from the same shared memory (or, for kept sets
-// larger than kFastDraw, from the lists in global memory).
+// larger than kFastDraw, from the lists in global memory).  Once a warp has
+// filtered its row of a wave it starts copying its row of the next wave
+// (survivor keys and count) into its scratch, so that a request going on
+// finds them there.
 template <bool BF16>
 __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScratch* scr,
                                  PostShared& sh) {
@@ -940,16 +987,24 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
   log2e_over_t(T, &chi, &clo);
   // the final draw's uniform, fetched while the waves run
   const float u_last = warp == 0 ? P.uniforms[t0 + k] : 0.f;
+  const Ws& w = P.ws;
   int w0 = 0;
+  int n_next = -1;  // survivor count of this warp's row of the next wave, being copied
   for (;; w0 += kWave) {
-    const int pos = w0 + (warp >> 1);
     float u = 0.f;  // warp 0: the uniform of position w0 + lane
     if (warp == 0 && lane < kWave && w0 + lane < k) u = P.uniforms[t0 + w0 + lane];
-    if (pos < k) {
-      const int64_t row = (warp & 1) ? P.Rt + d0 + pos : int64_t(t0) + pos;
-      warp_filter_row<BF16>(P, row, K, T, chi, clo, tp, P.draft_tokens[d0 + pos], scr[warp].sel);
-    } else if (warp == 2 * max(k - w0, 0)) {
-      warp_filter_row<BF16>(P, t0 + k, K, T, chi, clo, tp, -1, scr[warp].sel);
+    int gx;
+    const int64_t row = wave_row(P, b, t0, k, w0, warp, &gx);
+    if (row >= 0) {
+      if (n_next >= 0) copy_keys_wait();
+      warp_filter_row<BF16>(P, row, K, T, chi, clo, tp, gx, scr[warp].sel, n_next);
+    }
+    int gn;
+    const int64_t nrow = wave_row(P, b, t0, k, w0 + kWave, warp, &gn);
+    n_next = -1;
+    if (nrow >= 0) {
+      copy_keys_async(w.cand_raw + size_t(nrow) * kRawCap, scr[warp].sel.keys);
+      n_next = max(__ldcg(&w.stats[nrow].kept), 0);
     }
     __syncthreads();
     if (warp == 0) {
@@ -977,6 +1032,7 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
     __syncthreads();
     if (sh.L >= 0) break;
   }
+  if (n_next >= 0) copy_keys_wait();  // copies land before the scratch is reused
   const int L = sh.L;
   if (warp == 0) {
     // the stopping position lies in the last wave: its target (or bonus) row
