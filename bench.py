@@ -242,75 +242,45 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def pipelined_e2e(host, compute, outs_h, steps, stream, dev, pg):
-    """Milliseconds per step of a serving loop fed from pinned host buffers:
-    every step copies its inputs host->device (on a copy stream, into one of
-    two device buffer sets), runs compute(device inputs) on `stream` and reads
-    its outputs back into the pinned buffers outs_h.  Step i + 1's copy
-    overlaps step i's compute; a buffer set is rewritten only after the
-    compute that read it."""
-    import torch
-    dbufs = [{k: torch.empty_like(t, device=dev) for k, t in host.items()} for _ in range(2)]
-    cs = torch.cuda.Stream(dev)
-    ready = [torch.cuda.Event() for _ in range(2)]
-    free = [torch.cuda.Event() for _ in range(2)]
-
-    def step(i):
-        buf = dbufs[i % 2]
-        with torch.cuda.stream(cs):
-            cs.wait_event(free[i % 2])
-            for k_, t in host.items():
-                buf[k_].copy_(t, non_blocking=True)
-            ready[i % 2].record(cs)
-        stream.wait_event(ready[i % 2])
-        outs = compute(buf)
-        free[i % 2].record(stream)
-        for o_h, o in zip(outs_h, outs):
-            o_h.copy_(o, non_blocking=True)
-
-    for e in free:
-        e.record(stream)
-    for i in range(2):
-        step(i)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    cs.wait_event(e0)  # no copy of the timed steps starts before the clock
-    for i in range(steps):
-        step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = max_over_ranks(e0.elapsed_time(e1) / steps, pg, dev)
-    del dbufs
-    return ms
-
-
 def measure_e2e(args, batch, v, acc, tok, stream, dev, pg):
     """Same metric through the public API from pinned host buffers: every step
-    copies the step's inputs host->device and reads the results back
-    (pipelined: the next step's copy overlaps this step's verification)."""
+    copies the step's inputs host->device and reads the results back."""
     import torch
     ws = pg.get_world_size() if pg else 1
     B, Rt = batch.batch, batch.target_rows
     host = {k: getattr(batch, k).to("cpu").pin_memory() for k in
             ("target", "draft", "draft_tokens", "k_per_req", "temperature", "top_k", "top_p",
              "uniforms")}
+    dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
     acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
     tok_h = torch.empty(Rt, dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = acc_h.numel() * 4 + tok_h.numel() * 4
 
-    def compute(d):
-        return v(d["target"], d["draft"], d["draft_tokens"], d["k_per_req"], d["temperature"],
-                 d["uniforms"], d["top_k"], d["top_p"], out_accept_len=acc, out_tokens=tok)
+    def e2e_step():
+        for k_, t in host.items():
+            dbuf[k_].copy_(t, non_blocking=True)
+        a, o = v(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["k_per_req"],
+                 dbuf["temperature"], dbuf["uniforms"], dbuf["top_k"], dbuf["top_p"],
+                 out_accept_len=acc, out_tokens=tok)
+        acc_h.copy_(a, non_blocking=True)
+        tok_h.copy_(o, non_blocking=True)
 
-    e2e_ms = pipelined_e2e(host, compute, (acc_h, tok_h), args.e2e_steps, stream, dev, pg)
-    del host
+    for _ in range(2):
+        e2e_step()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, pg, dev)
+    del dbuf, host
     return {"value": ws * Rt / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms,
-            "pipelined": "step i+1's host->device copy overlaps step i's verification"}
+            "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "ms_per_step": e2e_ms}
 
 
 SAMPLE_METRIC = "draft-sampler rows/s at B=256,k=15,V=151936 bf16 (top-k 50, top-p 0.9)"
@@ -376,18 +346,32 @@ def run_sampler(args, ws, rank, local):
     if not args.no_e2e:
         host = {n: t.to("cpu").pin_memory() for n, t in
                 (("x", x), ("k", k), ("T", T), ("tk", tk), ("tp", tp), ("u", u))}
+        dbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
         tok_h = torch.empty(R, dtype=torch.int32).pin_memory()
 
-        def compute(d):
-            o, _ = s(d["x"], d["k"], d["T"], d["u"], d["tk"], d["tp"], out_tokens=tok)
-            return (o,)
+        def e2e_step():
+            for n, t in host.items():
+                dbuf[n].copy_(t, non_blocking=True)
+            o, _ = s(dbuf["x"], dbuf["k"], dbuf["T"], dbuf["u"], dbuf["tk"], dbuf["tp"],
+                     out_tokens=tok)
+            tok_h.copy_(o, non_blocking=True)
 
-        ms = pipelined_e2e(host, compute, (tok_h,), args.e2e_steps, stream, dev, pg)
+        for _ in range(2):
+            e2e_step()
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, pg, dev)
         e2e = {"value": ws * R / (ms * 1e-3), "unit": "rows/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
-               "d2h_bytes_per_step": R * 4, "steps": args.e2e_steps, "ms_per_step": ms,
-               "pipelined": "step i+1's host->device copy overlaps step i's sampling"}
-        del host
+               "d2h_bytes_per_step": R * 4, "steps": args.e2e_steps, "ms_per_step": ms}
+        del host, dbuf
     if rank != 0:
         if pg:
             pg.destroy_process_group()
