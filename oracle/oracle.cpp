@@ -25,8 +25,7 @@
 //         min(1, p/q); residual = positive part of p - q; top-k / top-p applied
 //         identically to both distributions).
 //
-// Readings where the pages leave a step open (each one is also listed in
-// the design doc):
+// Readings where the pages leave a step open:
 //   R1  accept iff u < p/q (the pages write r <= min(1, p/q); the two differ on
 //       a set of measure zero; with u in [0,1) this never accepts p = 0 and
 //       always accepts p >= q).
