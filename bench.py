@@ -99,17 +99,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (profiling recipe, 6.8 TB/s)"
 
 
-def recorded_traffic(bytes_per_launch):
-    """DRAM bytes per row-pass launch from the committed ncu summary, only if
-    it was taken on the current kernel source."""
+def recorded_traffic(rows, vocab):
+    """DRAM bytes of a row-pass launch over `rows` bf16 rows of `vocab` logits,
+    from the committed ncu summary: its per-row bytes (read + written) times
+    the rows, only if it was taken on the current kernel source and on rows
+    of the same length."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("kernel_hash") != kernel_hash():
+    if d.get("kernel_hash") != kernel_hash() or d.get("vocab") != vocab:
         return None
-    return d.get("dram_bytes_per_launch")
+    per_row = (d["dram_bytes_read_measured"] + d["dram_bytes_write_measured"]) / d["rows_measured"]
+    return per_row * rows
 
 
 class ClockSampler:
@@ -409,7 +412,10 @@ def run_sampler(args, ws, rank, local):
                    "parallelism": f"replicas x{ws} (independent batches)"},
         "hbm_gbs": bytes_per_step / (step_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "rowpass_kernel<bf16>", "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(R, V) if x.dtype == torch.bfloat16 else None,
+                     "traffic_source": "per-row DRAM bytes of the ncu capture of a B=64 "
+                                       "verification launch (top-k rows, same V), x rows",
                      "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
                      "launch_ms": rowpass_ms, "launches_timed": len(timed)},
         "e2e": e2e,
@@ -742,7 +748,7 @@ def main():
 
     peak, peak_src = measured_peak()
     achieved = bytes_per_step / (rowpass_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(bytes_per_step)
+    traffic = recorded_traffic(Rt + Rd, V) if batch.target.dtype == torch.bfloat16 else None
     cpu = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(batch)
