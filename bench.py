@@ -38,7 +38,7 @@ METRIC = "spec-verify rows/s and HBM GB/s vs ~8 TB/s peak at B=256,k=15,V=151936
 UNIT = "rows/s"
 WORKLOAD = "B=256 k=15 V=151936 bf16 logits, temperature 1, top-k 50 + top-p 0.9 on p and q"
 L2_NOTE = "inputs larger than L2 (2.41 GB of logits vs 129 MB), no flush"
-EVENT_EVERY = 4  # timed steps per row-pass event pair
+EVENT_EVERY = 8  # timed steps per row-pass event pair
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rowpass_c4_traffic.json")
 KERNEL_SOURCES = ["sv_internal.cuh", "sv_select.cuh", "sv_rowpass.cu"]
