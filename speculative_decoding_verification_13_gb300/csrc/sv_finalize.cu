@@ -206,6 +206,27 @@ __device__ __forceinline__ float weight_split(float v, float v0, float chi, floa
   return ex2_approx(ah - fl) * fmaf(al, 0.6931471805599453f, 1.0f);
 }
 
+// ceil(W * p) for 0 < p < 1 (a float), exactly: p = m 2^-s with m < 2^24 and
+// s >= 24, and W * m has at most 88 bits.
+__device__ __forceinline__ unsigned long long ceil_mul_frac(unsigned long long W, float p) {
+  const uint32_t b = __float_as_uint(p);
+  const uint32_t E = b >> 23;
+  const unsigned long long m = E ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+  const int s = E ? 150 - int(E) : 149;
+  const unsigned long long lo = W * m, hi = __umul64hi(W, m);
+  unsigned long long q;
+  bool rem;
+  if (s < 64) {
+    q = (hi << (64 - s)) | (lo >> s);
+    rem = (lo & ((1ull << s) - 1ull)) != 0ull;
+  } else {
+    const int t = s - 64;
+    q = t < 64 ? (hi >> t) : 0ull;
+    rem = lo != 0ull || (t < 64 ? (hi & ((1ull << t) - 1ull)) != 0ull : hi != 0ull);
+  }
+  return q + (rem ? 1ull : 0ull);
+}
+
 // f * 2^n (f a positive normal float, n <= 0) as a multiple of 2^-55, truncated.
 __device__ __forceinline__ unsigned long long fix55(float f, int n) {
   const uint32_t b = __float_as_uint(f);
@@ -565,9 +586,15 @@ __device__ __noinline__ void warp_filter_row(const Problem& P, int64_t row, int 
   bool exact = false;
   if (tp < 1.0f) {
     for (int pass = 0; pass < 2; ++pass) {
+      // ceil(top_p * W): exactly in integers the first time (top_p = m 2^-s
+      // with a 24-bit m), in double on the double-precision redo
       unsigned long long lim = 0ull;
-      if (lane == 0) lim = static_cast<unsigned long long>(ceil(double(tp) * double(W)));
-      lim = __shfl_sync(kFull, lim, 0);
+      if (pass == 0) {
+        lim = ceil_mul_frac(W, tp);
+      } else {
+        if (lane == 0) lim = static_cast<unsigned long long>(ceil(double(tp) * double(W)));
+        lim = __shfl_sync(kFull, lim, 0);
+      }
       int c = 0;
       for (int j0 = 0; j0 < nsel; j0 += 32) {
         const int j = j0 + lane;
@@ -985,8 +1012,10 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
   const float tp = P.top_p ? P.top_p[b] : 1.0f;
   float chi, clo;  // once per request
   log2e_over_t(T, &chi, &clo);
-  // the final draw's uniform, fetched while the waves run
+  // the final draw's uniform and the drafted tokens (lane i: token i),
+  // fetched while the waves run
   const float u_last = warp == 0 ? P.uniforms[t0 + k] : 0.f;
+  const int x_lane = warp == 0 && lane < k ? P.draft_tokens[d0 + lane] : -1;
   const Ws& w = P.ws;
   int w0 = 0;
   int n_next = -1;  // survivor count of this warp's row of the next wave, being copied
@@ -1046,8 +1075,8 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScr
       y = draw_fast(ts, residual ? &scr[tw + 1].sel : nullptr, u, sh.idx, sh.r, nullptr);
     else
       y = draw_kept(P, t0 + L, P.Rt + d0 + L, residual, u, scr[0].draw);
-    for (int i = lane; i <= k; i += 32)
-      P.out_tokens[t0 + i] = i < L ? P.draft_tokens[d0 + i] : (i == L ? y : -1);
+    if (lane <= k) P.out_tokens[t0 + lane] = lane < L ? x_lane : (lane == L ? y : -1);
+    if (lane == 0 && k == 32) P.out_tokens[t0 + 32] = L == 32 ? y : -1;
     if (P.out_pq)
       for (int i = L + 1 + lane; i < k; i += 32) {
         P.out_pq[2 * int64_t(d0 + i)] = nan64();
