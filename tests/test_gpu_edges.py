@@ -67,6 +67,23 @@ def test_many_requests_several_setup_chunks():
     check(b, "B=2500")
 
 
+@pytest.mark.parametrize("B", [1024, 1025])
+def test_setup_chunk_boundary(B):
+    """B = 1024 is the largest batch the setup kernel handles in one chunk
+    (eight CTAs sharing the row-list writes); B = 1025 takes two chunks (one
+    CTA).  Mixed greedy, unfiltered and filtered requests, k from 0 to 4."""
+    rng = np.random.default_rng(B)
+    k = rng.integers(0, 5, B)
+    kind = rng.integers(0, 3, B)
+    T = np.where(kind == 0, 0.0, rng.uniform(0.5, 1.5, B))
+    tk = np.where(kind == 2, rng.integers(1, 40, B), 0)
+    tp = np.where(kind == 2, rng.uniform(0.5, 1.0, B), 1.0)
+    b = W.make_batch_from_params(f"B={B}", k.tolist(), T.tolist(), [0.8] * B, 512,
+                                 torch.float32, B, device=DEV, top_k=tk.tolist(),
+                                 top_p=tp.tolist())
+    check(b, f"B={B}")
+
+
 def test_empty_batch_on_device():
     V = 1000
     target = torch.zeros(0, V, dtype=torch.bfloat16, device=DEV)

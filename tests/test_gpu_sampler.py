@@ -110,6 +110,20 @@ def test_many_requests_several_setup_chunks():
     assert code == 0
 
 
+@pytest.mark.parametrize("B", [1024, 1025])
+def test_setup_chunk_boundary(B):
+    """The sampler's setup at the largest one-chunk batch and one past it."""
+    rng = np.random.default_rng(B + 3)
+    k = rng.integers(0, 4, B).tolist()
+    kind = rng.integers(0, 3, B)
+    T = np.where(kind == 0, 0.0, rng.uniform(0.5, 1.5, B)).tolist()
+    tk = np.where(kind == 2, rng.integers(1, 30, B), 0).tolist()
+    tp = np.where(kind == 2, rng.uniform(0.5, 1.0, B), 1.0).tolist()
+    code, _, _ = check(sample_case(f"B={B}", k, T, 700, torch.float32, B, top_k=tk, top_p=tp),
+                       f"B={B}")
+    assert code == 0
+
+
 def test_data_errors_fail_their_requests_only():
     k = [2, 3, 2, 1]
     x, kk, T, tk, tp, u = sample_case("errors", k, [1.0, 1.0, 0.8, 1.0], 500, torch.float32, 36)
