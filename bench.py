@@ -36,9 +36,37 @@ sys.path.insert(0, ROOT)
 
 METRIC = "spec-verify rows/s and HBM GB/s vs ~8 TB/s peak at B=256,k=15,V=151936 bf16"
 UNIT = "rows/s"
-WORKLOAD = "B=256 k=15 V=151936 bf16 logits, temperature 1, top-k 50 + top-p 0.9 on p and q"
-L2_NOTE = "inputs larger than L2 (2.41 GB of logits vs 129 MB), no flush"
 EVENT_EVERY = 8  # timed steps per row-pass event pair
+L2_BYTES = 129 * 1000 * 1000
+FLUSH_BYTES = 512 << 20  # written between steps when the inputs fit in L2
+
+
+def workload_desc(config, variant, batch=None):
+    """The workload's name: its sizes and distributions, as the bench line
+    reports them."""
+    from speculative_decoding_verification_13_gb300 import workloads
+    c = workloads.CONFIGS[config]
+    B = c["B"] if batch is None else batch
+    dt = "bf16" if c["dtype"].is_floating_point and c["dtype"].itemsize == 2 else "fp32"
+    V = c["V"]
+    if config in ("c1", "c2"):
+        T = c["variants"][variant]
+        mode = "greedy (T=0)" if T == 0 else f"temperature {T}"
+        return (f"B={B} k={c['k']} V={V} {dt} logits, {mode}, draft = target + "
+                f"N(0,{c['sigma']}^2), no filter")
+    if config == "c3":
+        return (f"B={B} k={c['k']} V={V} {dt} logits, temperature {c['temp']}, draft = target "
+                f"+ N(0,{c['variants'][variant]}^2), no filter")
+    if config == "c4":
+        return (f"B={B} k={c['k']} V={V} {dt} logits, temperature 1, top-k {c['top_k']} + "
+                f"top-p {c['top_p']} on p and q")
+    if config == "c4p":
+        return (f"B={B} k={c['k']} V={V} {dt} logits, temperature 1, top-p {c['top_p']} alone "
+                f"on p and q (no top-k)")
+    if config == "c5":
+        return (f"B={B} ragged k~U{{1..15}} V={V} {dt} logits, 25% greedy else T~U[0.3,1.2], "
+                f"draft noise sigma~U[0.3,2] per request, no filter")
+    return config
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rowpass_c4_traffic.json")
 KERNEL_SOURCES = ["sv_internal.cuh", "sv_select.cuh", "sv_rowpass.cu"]
@@ -50,7 +78,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c4")
+    ap.add_argument("--config", default="c4",
+                    help="workload: c1..c5 (c4 = the headline), c4p = c4 with top-p alone")
+    ap.add_argument("--variant", default=None,
+                    help="c1/c2: t1|t0.7|greedy; c3: s0.5|s1|s2 (default: the first)")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the one-step comparison with the oracle after timing")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -208,8 +241,9 @@ def run_reference(args, ws, rank):
     oracle.build()
     cores = os.cpu_count() or 1
     B = workloads.CONFIGS[args.config]["B"]
+    variant = args.variant or next(iter(workloads.CONFIGS[args.config]["variants"]))
     gen = "cuda" if torch.cuda.is_available() else "cpu"
-    full = workloads.make_batch(args.config, device=gen, batch=min(B, cores))
+    full = workloads.make_batch(args.config, variant, device=gen, batch=min(B, cores))
     # a bounded sample per step: one request per host thread, shrunk to a
     # single request when K + W steps would otherwise exceed ~150 s
     n = min(B, cores)
@@ -235,7 +269,8 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded Zipf-plus-Gaussian logits, see workloads.py)",
-        "config": {"workload": WORKLOAD, "sample_requests": n, "global_batch": B},
+        "config": {"workload": workload_desc(args.config, variant), "name": f"{args.config}:{variant}",
+                   "sample_requests": n, "global_batch": B},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{n} requests ({sub.target_rows} verified rows) of the same "
                                    f"workload per step, per-request parallel over {cores} "
@@ -663,6 +698,39 @@ def run_lmhead(args, ws, rank, local):
         pg.destroy_process_group()
 
 
+def required_bytes(batch):
+    """Logit bytes the verification must read: every row of a sampled request,
+    the target rows only of a greedy request (its draft rows are never read)."""
+    k = batch.k_per_req.cpu().long()
+    sampled = batch.temperature.cpu() > 0
+    rows = int((k + 1).sum()) + int((k * sampled).sum())
+    return rows * batch.vocab * batch.target.element_size(), rows
+
+
+def parity_vs_oracle(batch, acc, tok, pq):
+    """One verified step of the timed batch against the oracle (outside the
+    timed region): counts of exempt requests and of mismatches, by the parity
+    rule of oracle/compare.py."""
+    import oracle
+    from oracle.compare import compare
+    import torch
+    oracle.build()
+    cpu = batch.to("cpu")
+    t0 = time.perf_counter()
+    o = oracle.verify(cpu.target, cpu.draft, cpu.draft_tokens, cpu.k_per_req, cpu.temperature,
+                      cpu.top_k, cpu.top_p, cpu.uniforms, threads=os.cpu_count() or 1)
+    dt = time.perf_counter() - t0
+    g = dict(acc=acc.cpu().numpy(), tok=tok.cpu().numpy(),
+             pq=pq[:batch.draft_rows].cpu().numpy() if pq is not None else None)
+    dtn = "bfloat16" if cpu.target.dtype == torch.bfloat16 else "float32"
+    rep = compare(cpu.k_per_req.numpy(), cpu.temperature.numpy(), cpu.vocab,
+                  cpu.draft_tokens.numpy(), dtn, g, o, batch.name)
+    out = rep.summary()
+    out["pass"] = rep.ok()
+    out["oracle_s"] = dt
+    return out
+
+
 def main():
     args = parse()
     ws, rank, local = dist_env()
@@ -696,9 +764,16 @@ def main():
         pg.barrier()
     sv.load_library()
 
-    batch = workloads.make_batch(args.config, device=dev, seed_offset=rank, batch=args.batch)
+    cfg = workloads.CONFIGS[args.config]
+    variant = args.variant or next(iter(cfg["variants"]))
+    batch = workloads.make_batch(args.config, variant, device=dev, seed_offset=rank,
+                                 batch=args.batch)
     B, Rt, Rd, V = batch.batch, batch.target_rows, batch.draft_rows, batch.vocab
-    bytes_per_step = batch.logit_bytes()
+    bytes_formula = batch.logit_bytes()
+    bytes_req, rows_req = required_bytes(batch)
+    # the inputs of the small workloads fit in L2: flush it between steps
+    flush = bytes_formula < 2 * L2_BYTES
+    scratch = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
     v = sv.Verifier(dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     tok = torch.empty(Rt, dtype=torch.int32, device=dev)
@@ -719,21 +794,32 @@ def main():
     # EVENT_EVERY-th step: an event recorded between two kernels ends the
     # overlap of one kernel's launch with the previous one's tail (about 8 us a
     # step on the bench workload), so bracketing every step would charge that
-    # measurement cost to the step time.
+    # measurement cost to the step time.  With an L2 flush between steps each
+    # step is bracketed by its own events (the flush is not timed).
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            if i % EVENT_EVERY == 0 else None for i in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)] if flush else None
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
     start.record(stream)
     for i in range(args.steps):
+        if flush:
+            scratch.fill_(i & 255)
+            steps_ev[i][0].record(stream)
         call(evs[i])
+        if flush:
+            steps_ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
-    step_ms = start.elapsed_time(end) / args.steps
+    if flush:
+        step_ms = sum(a.elapsed_time(b) for a, b in steps_ev) / args.steps
+    else:
+        step_ms = start.elapsed_time(end) / args.steps
     timed = [e for e in evs if e is not None]
     rowpass_ms = sum(a.elapsed_time(b) for a, b in timed) / len(timed)
     clk = clocks.stop() if clocks else None
@@ -747,11 +833,19 @@ def main():
         return
 
     peak, peak_src = measured_peak()
-    achieved = bytes_per_step / (rowpass_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(Rt + Rd, V) if batch.target.dtype == torch.bfloat16 else None
+    achieved = bytes_req / (rowpass_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(rows_req, V) \
+        if batch.target.dtype == torch.bfloat16 and args.config in ("c4",) else None
     cpu = None
+    parity = None
     if ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(batch)
+    if ws == 1 and not args.no_parity:
+        pq = torch.full((max(Rd, 1), 2), float("nan"), dtype=torch.float64, device=dev)
+        a1, t1 = v(batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
+                   batch.temperature, batch.uniforms, batch.top_k, batch.top_p, out_pq=pq)
+        parity = parity_vs_oracle(batch, a1, t1, pq)
+    dtype = "bf16" if batch.target.dtype == torch.bfloat16 else "f32"
     line = {
         "metric": METRIC,
         "value": ws * Rt / (step_ms * 1e-3),
@@ -763,22 +857,34 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": dtype,
         "data": "synthetic (seeded Zipf-plus-Gaussian logits, see workloads.py)",
-        "config": {"workload": WORKLOAD, "global_batch": ws * B, "per_gpu_batch": B,
-                   "k": 15, "vocab": V, "verified_rows_per_step": Rt,
-                   "logit_rows_per_step": Rt + Rd, "logit_bytes_per_step": bytes_per_step,
-                   "l2": L2_NOTE, "parallelism": f"replicas x{ws} (independent batches)"},
-        "hbm_gbs": bytes_per_step / (step_ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "rowpass_kernel<bf16>", "achieved": achieved,
+        "config": {"workload": workload_desc(args.config, variant, args.batch),
+                   "name": f"{args.config}:{variant}",
+                   "global_batch": ws * B, "per_gpu_batch": B,
+                   "k": cfg["k"] if cfg["k"] is not None else "U{1..15}",
+                   "vocab": V, "verified_rows_per_step": Rt,
+                   "logit_rows_per_step": Rt + Rd, "logit_bytes_per_step": bytes_formula,
+                   "required_logit_rows_per_step": rows_req,
+                   "required_logit_bytes_per_step": bytes_req,
+                   "l2": (f"inputs ({bytes_formula / 1e6:.1f} MB) fit in L2: a "
+                          f"{FLUSH_BYTES >> 20} MB buffer is written before every step, "
+                          f"outside the per-step events" if flush else
+                          f"inputs larger than L2 ({bytes_formula / 1e9:.2f} GB of logits vs "
+                          f"129 MB), no flush"),
+                   "parallelism": f"replicas x{ws} (independent batches)"},
+        "hbm_gbs": bytes_req / (step_ms * 1e-3) / 1e9,
+        "hbm_gbs_formula": bytes_formula / (step_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": f"rowpass_kernel<{dtype}>", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": peak_src,
-                     "bytes_per_launch": bytes_per_step, "launch_ms": rowpass_ms,
+                     "bytes_per_launch": bytes_req, "launch_ms": rowpass_ms,
                      "launches_timed": len(timed)},
         "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
+        "parity": parity,
     }
     print(json.dumps(line), flush=True)
     if pg:

@@ -171,6 +171,40 @@ def _check(t, name, dtype, ndim=1):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_verify_args(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k,
+                       top_p, out_accept_len, out_tokens, out_pq, Rt, Rd):
+    """Lengths, dtypes and devices of spec_verify's arguments, checked before
+    the call: the library reads and writes these buffers on the GPU with the
+    lengths that B, R_t and R_d imply, so a short or misplaced tensor would be
+    read or written past its end."""
+    B = int(k_per_req.numel())
+    dev = target.device
+    need = {"k_per_req": (k_per_req, B), "temperature": (temperature, B),
+            "uniforms": (uniforms, Rt), "draft_tokens": (draft_tokens, Rd),
+            "top_k": (top_k, B), "top_p": (top_p, B),
+            "out_accept_len": (out_accept_len, B), "out_tokens": (out_tokens, Rt)}
+    for name, (t, n) in need.items():
+        if t is None:
+            if name == "draft_tokens" and Rd == 0:
+                continue
+            if name in ("top_k", "top_p"):
+                continue
+            raise ValueError(f"{name} is required")
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the logits on {dev}")
+        if t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, {n} are needed")
+    if draft is not None and draft.device != dev:
+        raise ValueError(f"draft logits are on {draft.device}, the target logits on {dev}")
+    if out_pq is not None:
+        if not isinstance(out_pq, torch.Tensor) or out_pq.device != dev:
+            raise ValueError("out_pq must be a CUDA tensor on the logits' device")
+        if out_pq.dtype != torch.float64 or not out_pq.is_contiguous():
+            raise TypeError("out_pq must be a contiguous float64 tensor")
+        if out_pq.numel() < 2 * Rd:
+            raise ValueError(f"out_pq holds {out_pq.numel()} elements, {2 * Rd} are needed")
+
+
 def _logits_desc(x, V=None):
     if x is None:
         return _Logits(None, SV_BF16, V or 0, 0, V or 0)
@@ -229,16 +263,23 @@ class Verifier:
             out_tokens = torch.empty(Rt, dtype=torch.int32, device=target.device)
         _check(out_accept_len, "out_accept_len", torch.int32)
         _check(out_tokens, "out_tokens", torch.int32)
-        ws = self._workspace(B, Rt, Rd)
-        opts = None
-        if out_pq is not None or rowpass_events is not None:
-            ev0, ev1 = rowpass_events if rowpass_events is not None else (None, None)
-            opts = _Options(_ptr(out_pq), _event_handle(ev0, stream), _event_handle(ev1, stream))
-        rc = lib.spec_verify(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
-                             _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
-                             _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
-                             _stream_handle(stream), B, _ptr(ws), ws.numel(),
-                             ctypes.byref(opts) if opts is not None else None)
+        _check_verify_args(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k,
+                           top_p, out_accept_len, out_tokens, out_pq, Rt, Rd)
+        if self.workspace is not None and self.workspace.device != target.device:
+            raise ValueError(f"this Verifier's workspace is on {self.workspace.device}, "
+                             f"the logits on {target.device}")
+        with torch.cuda.device(target.device):
+            ws = self._workspace(B, Rt, Rd)
+            opts = None
+            if out_pq is not None or rowpass_events is not None:
+                ev0, ev1 = rowpass_events if rowpass_events is not None else (None, None)
+                opts = _Options(_ptr(out_pq), _event_handle(ev0, stream),
+                                _event_handle(ev1, stream))
+            rc = lib.spec_verify(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
+                                 _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
+                                 _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
+                                 _stream_handle(stream), B, _ptr(ws), ws.numel(),
+                                 ctypes.byref(opts) if opts is not None else None)
         if rc != SV_OK:
             raise SpecVerifyError(rc, "spec_verify")
         return out_accept_len, out_tokens
@@ -508,12 +549,17 @@ def verify_noalloc(target, draft, draft_tokens, k_per_req, temperature, uniforms
     if draft is None:
         dd.rows = td.rows - B
         dd.dtype = td.dtype
+    _check_verify_args(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k,
+                       top_p, out_accept_len, out_tokens, out_pq, int(td.rows), int(dd.rows))
     opts = _Options(_ptr(out_pq), None, None) if out_pq is not None else None
-    rc = lib.spec_verify_noalloc(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
-                                 _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
-                                 _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
-                                 _stream_handle(stream), B,
-                                 ctypes.byref(opts) if opts is not None else None)
+    # the library looks up the buffer of the current device: make it the
+    # logits' device
+    with torch.cuda.device(target.device):
+        rc = lib.spec_verify_noalloc(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
+                                     _ptr(k_per_req), _ptr(temperature), _ptr(top_k),
+                                     _ptr(top_p), _ptr(uniforms), _ptr(out_accept_len),
+                                     _ptr(out_tokens), _stream_handle(stream), B,
+                                     ctypes.byref(opts) if opts is not None else None)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_noalloc")
     return out_accept_len, out_tokens

@@ -104,6 +104,10 @@ CONFIGS = {
                variants={"s0.5": 0.5, "s1": 1.0, "s2": 2.0}),
     "c4": dict(B=256, k=15, V=VOCAB_QWEN3, dtype=torch.bfloat16, temp=1.0, sigma=1.0,
                top_k=50, top_p=0.9, seed=1304, variants={"default": None}),
+    # c4 with top-p alone (no top-k): the nucleus of a Zipf row then holds
+    # thousands of tokens
+    "c4p": dict(B=256, k=15, V=VOCAB_QWEN3, dtype=torch.bfloat16, temp=1.0, sigma=1.0,
+                top_k=0, top_p=0.9, seed=1306, variants={"default": None}),
     "c5": dict(B=1024, k=None, V=VOCAB_QWEN3, dtype=torch.bfloat16, seed=1305,
                variants={"default": None}),
 }
@@ -148,8 +152,19 @@ def _sample_draft_tokens(draft, temps, top_k, top_p, owner, g, chunk):
         on = (tk > 0) & (tk < V)
         n_on = int(on.sum().item())
         samp = None
-        if n_on < r1 - r0:  # rows without top-k: the whole softmax
-            samp = torch.multinomial(torch.softmax(z, dim=1), 1, generator=g).squeeze(1)
+        if n_on < r1 - r0:  # rows without top-k: the whole softmax, then top-p
+            pr = torch.softmax(z, dim=1)
+            if bool(((tp < 1) & ~on).any()):
+                # nucleus over the whole row: sort (logit desc, index asc),
+                # keep while the mass before a token is below top_p
+                order = torch.argsort(z, dim=1, descending=True, stable=True)
+                ps = pr.gather(1, order)
+                before = torch.cumsum(ps, dim=1) - ps
+                keep = before < tp[:, None]
+                ps = torch.where(keep, ps, torch.zeros_like(ps))
+                pr = torch.zeros_like(pr).scatter_(1, order, ps)
+                del order, ps, before, keep
+            samp = torch.multinomial(pr, 1, generator=g).squeeze(1)
         if n_on:
             kk = int(torch.where(on, tk, torch.zeros_like(tk)).max().item())
             vals, idx = torch.topk(z, kk, dim=1)
@@ -233,7 +248,7 @@ def make_batch(config: str, variant: str | None = None, device="cpu", batch: int
         sigma = c["variants"][variant]
         return make_batch_from_params(name, [c["k"]] * B, [c["temp"]] * B, [sigma] * B, V,
                                       dtype, seed, device)
-    if config == "c4":
+    if config in ("c4", "c4p"):
         return make_batch_from_params(name, [c["k"]] * B, [c["temp"]] * B, [c["sigma"]] * B,
                                       V, dtype, seed, device, top_k=[c["top_k"]] * B,
                                       top_p=[c["top_p"]] * B)

@@ -40,3 +40,30 @@ def test_traffic_withheld_for_another_kernel_or_row_length(tmp_path, monkeypatch
     monkeypatch.setattr(bench, "PROFILE_TRAFFIC", str(tmp_path / "missing.json"))
     assert bench.recorded_traffic(100, d["vocab"]) is None
 
+
+
+def test_workload_names_follow_the_config():
+    """Each config's line names its own workload (sizes, dtype, filter)."""
+    assert "B=256 k=15 V=151936 bf16" in bench.workload_desc("c4", "default")
+    assert "top-k 50 + top-p 0.9" in bench.workload_desc("c4", "default")
+    assert "top-p 0.9 alone" in bench.workload_desc("c4p", "default")
+    assert "B=1 k=4 V=1024 fp32" in bench.workload_desc("c1", "t1")
+    assert "greedy" in bench.workload_desc("c2", "greedy")
+    assert "N(0,2.0^2)" in bench.workload_desc("c3", "s2")
+    assert "ragged" in bench.workload_desc("c5", "default")
+    assert "B=64" in bench.workload_desc("c4", "default", batch=64)
+
+
+def test_required_bytes_skip_greedy_draft_rows():
+    """Greedy requests read their target rows only; sampled ones every row."""
+    from speculative_decoding_verification_13_gb300 import workloads
+    b = workloads.make_batch_from_params("t", [3, 2, 4], [1.0, 0.0, 0.5], [1.0] * 3, 64,
+                                         bench_dtype(), 5)
+    nbytes, rows = bench.required_bytes(b)
+    assert rows == (4 + 3 + 5) + (3 + 4)
+    assert nbytes == rows * 64 * 4
+
+
+def bench_dtype():
+    import torch
+    return torch.float32

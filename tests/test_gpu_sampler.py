@@ -1,7 +1,8 @@
 """Draft-side sampler on the GPU against the oracle, element by element on the
 same seeded rows and uniforms: tokens bit-exact except where the oracle's own
-decision margin is below the rounding of a float implementation (CDF margin
-< 1e-5, top-p margin < 1e-12), q(x) within the probability tolerance."""
+decision margin is below the rounding of a float implementation (a CDF
+margin of the draw or of the top-p cut below 1e-5), with such excused
+mismatches at most 1e-4 of the rows; q(x) within the probability tolerance."""
 
 import numpy as np
 import pytest
@@ -9,6 +10,7 @@ import torch
 
 import oracle
 import speculative_decoding_verification_13_gb300 as sv
+from oracle.compare import MARGIN, MAX_EXCUSED_FRAC
 from speculative_decoding_verification_13_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -37,12 +39,14 @@ def check(case, name, threads=16):
                             threads=threads)
     tok, q = tok.cpu().numpy(), q.cpu().numpy()
     R = tok.shape[0]
-    exempt = (o["margins"][:, 0] < 1e-5) | (o["margins"][:, 1] < 1e-12)
+    exempt = (o["margins"][:, 0] < MARGIN) | (o["margins"][:, 1] < MARGIN)
     mism = tok != o["tokens"]
     bad = np.nonzero(mism & ~exempt)[0]
+    excused = int((mism & exempt).sum())
     print(f"{name}: {R} rows, exempt {int(exempt.sum())}, mismatches non-exempt {len(bad)} "
-          f"exempt {int((mism & exempt).sum())}")
+          f"excused {excused}")
     assert len(bad) == 0, f"non-exempt mismatches at rows {bad[:10]}"
+    assert excused <= MAX_EXCUSED_FRAC * R, f"excused mismatches {excused} of {R} rows"
     same = ~mism
     tol = 2e-3 if x.dtype == torch.bfloat16 else 1e-5
     oq = o["q"][same]

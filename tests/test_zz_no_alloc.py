@@ -3,8 +3,10 @@
 kernels, so emitted tokens and accept lengths must agree exactly and (p, q)
 within the floating-point tolerance of the parity tests; each case makes two
 allocation-free calls in a row so that state left in the shared buffer by one
-call cannot leak into the next.  Collected last on purpose: it must pass alone
-and after every other test in the session."""
+call cannot leak into the next, and the buffer is filled with 0xFF bytes
+before the first of them (nothing in it has to start at zero).  Collected
+last on purpose: it must pass alone and after every other test in the
+session."""
 
 import pytest
 import torch
@@ -37,6 +39,8 @@ def test_noalloc_matches_workspace_path(config, variant, batch):
     acc0, tok0, pq0 = _outputs(b, dev)
     sv.Verifier(dev)(*args, out_accept_len=acc0, out_tokens=tok0, out_pq=pq0)
     torch.cuda.synchronize()
+    # the buffer is documented to need no zeroing: fill it with junk first
+    _fill_scratch(0xFF)
     for _ in range(2):
         acc1, tok1, pq1 = _outputs(b, dev)
         sv.verify_noalloc(*args, out_accept_len=acc1, out_tokens=tok1, out_pq=pq1)
@@ -52,6 +56,22 @@ def test_noalloc_matches_workspace_path(config, variant, batch):
         tol = PQ_RTOL[b.target.dtype]
         ok = ~nan0
         assert torch.allclose(pq1[ok], pq0[ok], rtol=tol, atol=0.0)
+
+
+def _fill_scratch(byte):
+    """Overwrite the library's whole buffer, seen through its device address
+    as a byte tensor (the CUDA array interface wraps the address; nothing is
+    allocated)."""
+    ptr, nbytes = sv.noalloc_scratch()
+
+    class _Raw:
+        __cuda_array_interface__ = {"shape": (nbytes,), "typestr": "|u1",
+                                    "data": (ptr, False), "version": 3}
+
+    view = torch.as_tensor(_Raw(), device="cuda")
+    assert view.data_ptr() == ptr and view.numel() == nbytes
+    view.fill_(byte)
+    torch.cuda.synchronize()
 
 
 class _ScratchView:
