@@ -454,7 +454,7 @@ def run_sampler(args, ws, rank, local):
                      "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
                      "launch_ms": rowpass_ms, "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -881,7 +881,7 @@ def main():
                      "bytes_per_launch": bytes_req, "launch_ms": rowpass_ms,
                      "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 5 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "parity": parity,

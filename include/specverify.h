@@ -69,8 +69,7 @@ extern "C" {
 #define SV_ERR_DATA_K 16            /* k_b outside [0, SV_MAX_K]                 */
 #define SV_ERR_DATA_TEMPERATURE 17  /* temperature negative, NaN or infinite     */
 #define SV_ERR_DATA_TOP_P 18        /* top_p outside (0, 1]                      */
-#define SV_ERR_DATA_TOP_K 19        /* top_k < 0, 0 < top_k < V with top_k >     */
-                                    /* SV_TOPK_MAX, or top-p without top-k        */
+#define SV_ERR_DATA_TOP_K 19        /* top_k < 0                                 */
 #define SV_ERR_DATA_TOKEN 20        /* a draft token outside [0, V)              */
 #define SV_ERR_DATA_ROWS 21         /* sum(k+1) != target rows or sum(k) !=      */
                                     /* draft rows (whole batch)                  */
@@ -85,7 +84,9 @@ extern "C" {
 
 /* ---- limits -------------------------------------------------------------- */
 #define SV_MAX_K 32              /* drafts per request (one warp ballot)       */
-#define SV_TOPK_MAX 256          /* largest active top-k                       */
+#define SV_TOPK_MAX 256          /* largest top-k whose kept set is listed     */
+                                 /* (spec_verify_dump_rows); larger top-k and   */
+                                 /* top-p alone keep a threshold instead        */
 #define SV_VOCAB_MAX (1 << 22)   /* largest vocabulary                         */
 
 typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -125,8 +126,10 @@ size_t spec_verify_workspace_size(int32_t batch, int64_t target_rows, int64_t dr
  *                  `data` may be NULL when every temperature is 0
  *   draft_tokens   [R_d] int32            k_per_req   [B] int32, 0..SV_MAX_K
  *   temperature    [B] float, 0 = greedy
- *   top_k          [B] int32 or NULL; 0 or >= V switches top-k off
- *   top_p          [B] float or NULL; 1 switches top-p off; (0, 1]
+ *   top_k          [B] int32 or NULL; 0 or >= V switches top-k off; any
+ *                  value in [1, V) is supported
+ *   top_p          [B] float or NULL; 1 switches top-p off; (0, 1]; top-k
+ *                  and top-p switch on and off independently
  *   uniforms       [R_t] float in [0, 1)
  *   out_accept_len [B] int32 (L, or -1 on a data error)
  *   out_tokens     [R_t] int32
@@ -150,17 +153,22 @@ int spec_verify_get_error(const void* workspace, void* stream, int32_t* code,
 /* Synchronises `stream` and copies the per-row intermediate results of the
  * last call into host buffers (test / debug use).  Rows are numbered target
  * rows first (0 .. R_t-1), then draft rows (R_t .. R_t+R_d-1).
- *   stats      [R, 4] doubles: row max logit, softmax normaliser (sampling rows:
- *              sum of exp((x - max)/T) for unfiltered rows, 0 for filtered),
- *              p(x) of the row's draft token (NaN if none), greedy argmax
- *              (-1 if not computed)
+ *   stats      [R, 5] doubles: row max logit, softmax normaliser (sampling rows:
+ *              sum of exp((x - max)/T) for unfiltered rows; the kept set's
+ *              sum for rows filtered by top-p alone or a top-k above
+ *              SV_TOPK_MAX; the kept weight for other filtered rows), p(x) of
+ *              the row's draft token (NaN if none), greedy argmax (-1 if not
+ *              computed), and the last kept token (in logit-descending,
+ *              index-ascending order) of a row filtered by top-p alone or a
+ *              top-k above SV_TOPK_MAX (-1 otherwise)
  *   kept_count [R] int32: size of the kept set after top-k / top-p (0 if the
  *              row was not filtered)
  *   kept_idx   [R, SV_TOPK_MAX] int32 and kept_p [R, SV_TOPK_MAX] doubles:
  *              the kept tokens in (logit desc, index asc) order and their
- *              renormalised probabilities.  Filtered requests evaluate only
- *              the rows up to their first rejection (and the bonus row after
- *              k acceptances); other rows' entries are unspecified.
+ *              renormalised probabilities, for rows whose top-k is active and
+ *              at most SV_TOPK_MAX.  Those requests evaluate only the rows up
+ *              to their first rejection (and the bonus row after k
+ *              acceptances); other rows' entries are unspecified.
  * Any output pointer may be NULL. */
 int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t batch,
                           int64_t target_rows, int64_t draft_rows, void* stream,

@@ -493,7 +493,7 @@ def get_error(workspace, stream=None):
 def dump_rows(workspace, batch, target_rows, draft_rows, stream=None):
     """Per-row intermediate results of the last call (host tensors)."""
     R = target_rows + draft_rows
-    stats = torch.empty(R, 4, dtype=torch.float64)
+    stats = torch.empty(R, 5, dtype=torch.float64)
     kept = torch.empty(R, dtype=torch.int32)
     kidx = torch.empty(R, SV_TOPK_MAX, dtype=torch.int32)
     kp = torch.empty(R, SV_TOPK_MAX, dtype=torch.float64)

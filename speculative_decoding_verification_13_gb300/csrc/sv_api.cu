@@ -1,7 +1,8 @@
 // Host side of the C ABI: argument validation, workspace layout, and the
-// four launches on the caller's stream: setup -> row pass -> filter / decide
-// -> draw pass for verification, sampler setup -> row pass -> sampler rows ->
-// draw pass for the draft-side sampler.
+// launches on the caller's stream: setup -> row pass over the rows not
+// filtered by a kept-set threshold -> row pass over those -> filter / decide
+// -> draw pass for verification; sampler setup -> the same two row passes ->
+// sampler rows -> draw pass for the draft-side sampler.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -142,7 +143,11 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   if (options && options->event_rowpass_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
     return SV_ERR_CUDA;
-  if (grid > 0 && launch_rowpass(P, t.dtype == SV_BF16, grid, s) != cudaSuccess)
+  // every row but those filtered by a kept-set threshold (top-p alone, large
+  // top-k), then those: the second launch's CTAs become resident in the
+  // first one's tail, so that it costs little when it has no rows
+  if (grid > 0 && (launch_rowpass(P, t.dtype == SV_BF16, false, grid, s) != cudaSuccess ||
+                   launch_rowpass(P, t.dtype == SV_BF16, true, grid, s) != cudaSuccess))
     return SV_ERR_CUDA;
   if (options && options->event_rowpass_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
@@ -223,7 +228,8 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   if (options && options->event_rowpass_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
     return SV_ERR_CUDA;
-  if (launch_rowpass(P, bf16, int(rows < ctas ? rows : ctas), s) != cudaSuccess)
+  if (launch_rowpass(P, bf16, false, int(rows < ctas ? rows : ctas), s) != cudaSuccess ||
+      launch_rowpass(P, bf16, true, int(rows < ctas ? rows : ctas), s) != cudaSuccess)
     return SV_ERR_CUDA;
   if (options && options->event_rowpass_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
@@ -341,14 +347,23 @@ int spec_verify_dump_rows(const void* workspace, size_t workspace_bytes, int32_t
     if (cudaMemcpy(st.data(), base + L.off_stats, R * sizeof(RowStat), cudaMemcpyDeviceToHost) !=
         cudaSuccess)
       return SV_ERR_CUDA;
+    // the kept-set thresholds of kBig rows (slot 0 of each row's survivors)
+    std::vector<uint64_t> th(R, 0ull);
+    for (size_t r = 0; r < R; ++r)
+      if (st[r].mode == kBig &&
+          cudaMemcpy(&th[r], base + L.off_raw + r * kRawCap * sizeof(uint64_t), sizeof(uint64_t),
+                     cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SV_ERR_CUDA;
     for (size_t r = 0; r < R; ++r) {
       if (stats) {
-        stats[4 * r + 0] = st[r].m;
-        stats[4 * r + 1] = st[r].s;
-        stats[4 * r + 2] = st[r].pg;
-        stats[4 * r + 3] = st[r].arg;
+        stats[5 * r + 0] = st[r].m;
+        stats[5 * r + 1] = st[r].s;
+        stats[5 * r + 2] = st[r].pg;
+        stats[5 * r + 3] = st[r].arg;
+        // the last kept token of a threshold-filtered row: ~ the key's low word
+        stats[5 * r + 4] = st[r].mode == kBig ? double(int32_t(~uint32_t(th[r]))) : -1.0;
       }
-      if (kept_count) kept_count[r] = st[r].mode == kTopk ? st[r].kept : 0;
+      if (kept_count) kept_count[r] = (st[r].mode == kTopk || st[r].mode == kBig) ? st[r].kept : 0;
     }
   }
   if (kept_idx && cudaMemcpy(kept_idx, base + L.off_cidx, R * kTopkMax * sizeof(int32_t),
@@ -374,7 +389,7 @@ const char* spec_verify_strerror(int code) {
     case SV_ERR_DATA_K: return "k_per_req outside [0, SV_MAX_K]";
     case SV_ERR_DATA_TEMPERATURE: return "temperature negative, NaN or infinite";
     case SV_ERR_DATA_TOP_P: return "top_p outside (0, 1]";
-    case SV_ERR_DATA_TOP_K: return "top_k negative, above SV_TOPK_MAX, or top-p without top-k";
+    case SV_ERR_DATA_TOP_K: return "top_k negative";
     case SV_ERR_DATA_TOKEN: return "draft token outside [0, V)";
     case SV_ERR_DATA_ROWS: return "row counts do not match k_per_req";
     case SV_ERR_DATA_LOGIT: return "NaN or +inf logit, or a sampled row without a finite logit";

@@ -1,8 +1,10 @@
-// Draw pass: the final token of every unfiltered sampled request, by inverse
+// Draw pass: the final token of every sampled request that is unfiltered or
+// filtered by a kept-set threshold (top-p alone, large top-k), by inverse
 // CDF in vocabulary-index order, y* = min{ y : C_y > u_k S }, over
 //   the normalised residual max(0, p_L - q_L) after a rejection at L
 //     ("FlashMap…" §4 step 3; "DFlash" §4), or
-//   p_k after a full acceptance (the bonus token).
+//   p_k after a full acceptance (the bonus token),
+// with p and q zero outside their rows' kept sets.
 //
 // Persistent CTAs, one queued request at a time per CTA.  As in the row pass,
 // warp 0 is a producer that streams the request's target row (and draft row,
@@ -36,15 +38,35 @@ constexpr uint32_t kFull = 0xffffffffu;
 //   kind 0: bonus, exp((x_t - m_t)/T)             (unnormalised p_k)
 //   kind 1: residual, max(0, p_t - q_t)
 //   kind 2: residual fallback, p_t
+// A row filtered by a threshold (top-p alone or a large top-k) keeps y iff
+// its composite key (logit descending, index ascending) is at least the
+// threshold's: x > v, or x == v and y <= i for the threshold's value v and
+// index i; p or q is 0 outside the kept set.
 struct Weights {
   float mt, ist, md, isd, c2;
   int kind;
+  bool mask_t, mask_d;
+  float vt, vd;
+  uint32_t it, id;
   __device__ __forceinline__ float operator()(float xt, float xd) const {
     const float et = ex2_approx((xt - mt) * c2);
     if (kind == 0) return et;
     if (kind == 2) return et * ist;
     const float ed = ex2_approx((xd - md) * c2);
     return fmaxf(0.f, et * ist - ed * isd);
+  }
+  // the same with the kept-set masks (y: the element's index)
+  __device__ __forceinline__ float masked(float xt, float xd, uint32_t y) const {
+    const bool kt = !mask_t || xt > vt || (xt == vt && y <= it);
+    const float et = kt ? ex2_approx((xt - mt) * c2) : 0.f;
+    if (kind == 0) return et;
+    if (kind == 2) return et * ist;
+    const bool kd = !mask_d || xd > vd || (xd == vd && y <= id);
+    const float ed = kd ? ex2_approx((xd - md) * c2) : 0.f;
+    return fmaxf(0.f, et * ist - ed * isd);
+  }
+  __device__ __forceinline__ float at(float xt, float xd, int y) const {
+    return (mask_t || mask_d) ? masked(xt, xd, uint32_t(y)) : (*this)(xt, xd);
   }
 };
 
@@ -249,7 +271,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     if (Wt.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
     float ls = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ls += Wt(xt[k], Wt.kind == 1 ? xd[k] : 0.f);
+    for (int k = 0; k < 8; ++k) ls += Wt.at(xt[k], Wt.kind == 1 ? xd[k] : 0.f, e + k);
     return __shfl_sync(kFull, warp_scan_f(ls), 31);
   };
   // sum of tiles [a, z) in tile order (double), one warp
@@ -271,6 +293,12 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     W.isd = d.isd;
     W.c2 = d.c2;
     W.kind = d.kind;
+    W.mask_t = d.kt != 0ull;
+    W.mask_d = d.kind == 1 && d.kd != 0ull;
+    W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
+    W.vd = W.mask_d ? composite_value(d.kd) : 0.f;
+    W.it = uint32_t(composite_index(d.kt));
+    W.id = uint32_t(composite_index(d.kd));
     const void* trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
     const void* drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
                                          (d.dr - P.Rt) * P.d_stride * E::kSize
@@ -295,8 +323,14 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
           elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
           if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
           float ls = 0.f;
+          if (W.mask_t || W.mask_d) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+            for (int k = 0; k < 8; ++k)
+              ls += W.masked(xt[k], W.kind == 1 ? xd[k] : 0.f, uint32_t(e + k));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+          }
           const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
           if (lane == 0) ts[tau] = tsum;
         }
@@ -432,7 +466,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
         float ls = 0.f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          r[k] = W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+          r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, base + k);
           ls += r[k];
         }
         const float inc = warp_scan_f(ls);

@@ -206,27 +206,6 @@ __device__ __forceinline__ float weight_split(float v, float v0, float chi, floa
   return ex2_approx(ah - fl) * fmaf(al, 0.6931471805599453f, 1.0f);
 }
 
-// ceil(W * p) for 0 < p < 1 (a float), exactly: p = m 2^-s with m < 2^24 and
-// s >= 24, and W * m has at most 88 bits.
-__device__ __forceinline__ unsigned long long ceil_mul_frac(unsigned long long W, float p) {
-  const uint32_t b = __float_as_uint(p);
-  const uint32_t E = b >> 23;
-  const unsigned long long m = E ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
-  const int s = E ? 150 - int(E) : 149;
-  const unsigned long long lo = W * m, hi = __umul64hi(W, m);
-  unsigned long long q;
-  bool rem;
-  if (s < 64) {
-    q = (hi << (64 - s)) | (lo >> s);
-    rem = (lo & ((1ull << s) - 1ull)) != 0ull;
-  } else {
-    const int t = s - 64;
-    q = t < 64 ? (hi >> t) : 0ull;
-    rem = lo != 0ull || (t < 64 ? (hi & ((1ull << t) - 1ull)) != 0ull : hi != 0ull);
-  }
-  return q + (rem ? 1ull : 0ull);
-}
-
 // f * 2^n (f a positive normal float, n <= 0) as a multiple of 2^-55, truncated.
 __device__ __forceinline__ unsigned long long fix55(float f, int n) {
   const uint32_t b = __float_as_uint(f);
@@ -745,10 +724,14 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
   d.ist = float(1.0 / st.s);
   d.md = 0.f;
   d.isd = 0.f;
+  // rows filtered by a threshold (kBig) draw from their kept sets only
+  d.kt = st.mode == kBig ? w.cand_raw[size_t(d.tr) * kRawCap] : 0ull;
+  d.kd = 0ull;
   if (L < k) {
     const RowStat sd = w.stats[d.dr];
     d.md = sd.m;
     d.isd = float(1.0 / sd.s);
+    d.kd = sd.mode == kBig ? w.cand_raw[size_t(d.dr) * kRawCap] : 0ull;
   }
   d.c2 = __fdiv_rn(1.4426950408889634f, T);
   d.kind = L < k ? 1 : 0;
@@ -1147,16 +1130,18 @@ __global__ void __launch_bounds__(kPostThreads, 2) sample_post_kernel(const Prob
     }
     return;
   }
-  const int n = w.hdr->n_active;
+  // rows listed from the front (hdr->n_active), then the kBig rows listed
+  // from the back (hdr->n_big)
+  const int na = w.hdr->n_active, n = na + w.hdr->n_big;
   WarpScratch& ws = scr[warp];
   for (;;) {
     int j = 0;
     if (lane == 0) j = atomicAdd(&w.hdr->next_row, 1);
     j = __shfl_sync(kFull, j, 0);
     if (j >= n) break;
-    const RowJob job = w.rowlist[j];
+    const RowJob job = j < na ? w.rowlist[j] : w.rowlist[P.Rt - 1 - (j - na)];
     const int64_t row = job.row;
-    const int mode = job.mode & 3;
+    const int mode = job.mode & kModeMask;
     const double u = double(P.uniforms[row]);
     int y = -1;
     float qy = __int_as_float(0x7fc00000);
@@ -1195,6 +1180,8 @@ __global__ void __launch_bounds__(kPostThreads, 2) sample_post_kernel(const Prob
         d.ist = float(1.0 / st.s);
         d.md = 0.f;
         d.isd = 0.f;
+        d.kt = mode == kBig ? w.cand_raw[size_t(row) * kRawCap] : 0ull;
+        d.kd = 0ull;
         d.c2 = __fdiv_rn(1.4426950408889634f, job.T);
         d.kind = 0;
         d.u = u;

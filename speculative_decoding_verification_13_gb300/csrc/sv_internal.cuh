@@ -27,8 +27,15 @@ constexpr int kTopkMax = SV_TOPK_MAX;
 constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
 constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
 
-// Row modes chosen per request by the setup kernel.
-enum RowMode : int { kSkip = 0, kStats = 1, kArgmax = 2, kTopk = 3 };
+// Row modes chosen per request by the setup kernel.  kTopk: a filtered row
+// whose top-k is active and at most SV_TOPK_MAX (candidates captured in one
+// pass, kept set materialised by the filter kernel); kBig: any other filtered
+// row (top-p alone, or a larger top-k), whose kept set is a threshold on the
+// composite key found by the row pass itself.
+enum RowMode : int { kSkip = 0, kStats = 1, kArgmax = 2, kTopk = 3, kBig = 4 };
+constexpr int kModeBits = 3;   // RowJob::mode = (position << kModeBits) | row mode
+constexpr int kModeMask = 7;
+constexpr int kBigPasses = 3;  // streams of a kBig row: max, histogram, collection
 
 // ---------------------------------------------------------------- workspace
 struct WsHeader {
@@ -42,11 +49,14 @@ struct WsHeader {
   int32_t n_draw;       // requests queued for the unfiltered draw
   int32_t next_row;     // draft sampler: rows handed out to warps so far
   int32_t rp_next;      // row pass: rows claimed past each CTA's first
-  int32_t pad[5];
+  int32_t n_big;        // kBig rows, listed from the end of the row list
+  int32_t rp_next_big;  // row pass over the kBig rows: rows claimed past each CTA's first
+  int32_t pad[3];
 };
 
 struct RowStat {
-  double s;     // softmax normaliser (sampling rows; kept-set weight for filtered rows)
+  double s;     // softmax normaliser (sampling rows; kept-set weight for filtered rows,
+                // relative to the row max m for kBig rows)
   double pg;    // p(x) of the row's draft token
   float m;      // row max logit
   int32_t arg;  // greedy argmax
@@ -63,6 +73,9 @@ struct DrawDesc {
   int32_t kind;    // 0 bonus p_k, 1 residual max(0, p_L - q_L), 2 residual fallback p_L
   double u;        // the final uniform u_k
   int32_t t0, L;
+  // kept sets of kBig rows: the element y of a row is kept iff its composite
+  // key is >= the row's threshold (0 keeps every element: unfiltered rows)
+  uint64_t kt, kd;
 };
 
 // One entry of the row pass's work list, in request order (setup kernel).
@@ -71,7 +84,7 @@ struct __align__(16) RowJob {
   int32_t row;   // target rows 0 .. R_t - 1, then draft rows R_t ..
   int32_t b;     // request
   int32_t gx;    // token whose probability the row reports, or -1
-  int32_t mode;  // (position << 2) | row mode
+  int32_t mode;  // (position << kModeBits) | row mode
   float T;       // the request's temperature
   int32_t K;     // the request's top-k (filtered rows)
   int32_t pad[2];
@@ -82,11 +95,14 @@ struct Ws {
   WsHeader* hdr;
   int32_t* t_off;    // [B + 1]
   int32_t* req_flag; // [B]
-  RowJob* rowlist;   // [R] rows the row pass streams
+  RowJob* rowlist;   // [R] rows the row pass streams: the hdr->n_active others
+                     // from the front, the hdr->n_big kBig rows from the back
+                     // (kBig row j at R - 1 - j)
   RowStat* stats;    // [R]
   int32_t* cand_idx; // [R, kTopkMax]
   float* cand_p;     // [R, kTopkMax] kept probabilities
-  uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys)
+  uint64_t* cand_raw; // [R, kRawCap] top-k survivors of the row pass (composite keys);
+                      // kBig rows: slot 0 holds the kept-set threshold key
   int4* job;          // [2B] {request, 0, t_off, k}: filtered requests from 0,
                       //      the other requests from B
   DrawDesc* draw;     // [B] queued draws, in queue order
@@ -169,7 +185,7 @@ struct Problem {
 
 // ------------------------------------------------------- host-side launchers
 cudaError_t launch_setup(const Problem& P, cudaStream_t s);
-cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_rowpass(const Problem& P, bool bf16, bool big, int grid, cudaStream_t s);
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
@@ -351,6 +367,27 @@ __device__ __forceinline__ float composite_value(uint64_t c) {
 
 __device__ __forceinline__ int32_t composite_index(uint64_t c) {
   return static_cast<int32_t>(~static_cast<uint32_t>(c));
+}
+
+// ceil(W * p) for 0 < p < 1 (a float), exactly: p = m 2^-s with m < 2^24 and
+// s >= 24, and W * m has at most 88 bits.
+__device__ __forceinline__ unsigned long long ceil_mul_frac(unsigned long long W, float p) {
+  const uint32_t b = __float_as_uint(p);
+  const uint32_t E = b >> 23;
+  const unsigned long long m = E ? ((b & 0x7fffffu) | 0x800000u) : (b & 0x7fffffu);
+  const int s = E ? 150 - int(E) : 149;
+  const unsigned long long lo = W * m, hi = __umul64hi(W, m);
+  unsigned long long q;
+  bool rem;
+  if (s < 64) {
+    q = (hi << (64 - s)) | (lo >> s);
+    rem = (lo & ((1ull << s) - 1ull)) != 0ull;
+  } else {
+    const int t = s - 64;
+    q = t < 64 ? (hi >> t) : 0ull;
+    rem = lo != 0ull || (t < 64 ? (hi & ((1ull << t) - 1ull)) != 0ull : hi != 0ull);
+  }
+  return q + (rem ? 1ull : 0ull);
 }
 
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int m) {

@@ -25,6 +25,9 @@
 //             redone exactly from global memory (certified radix selection).
 //             ("Speculative decoding and multi-token prediction", "Why the
 //             output is identical": the same filter on both distributions.)
+//   kBig    - a row filtered by top-p alone or by a top-k above SV_TOPK_MAX:
+//             streamed three times (max; histogram; the crossing bins), it
+//             ends with the kept set's threshold key and mass (sv_bigrow.cuh).
 // Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops
 // issuing copies, lets the copies it issued land, and exits.
 #include <math.h>
@@ -45,8 +48,17 @@ static_assert(kOffStage % 16 == 0, "staged vectors are 16-byte aligned");
 static_assert(kRowpassCtasPerSm * (kSmemBytes + 4096 + 1024) <= 228 * 1024,
               "shared memory budget for the resident CTAs of one SM");
 
+#include "sv_bigrow.cuh"
+
+// kBig rows use the candidate buffer and the selection scratch (contiguous)
+// as their work area: the histogram, then the band's keys.
+static_assert(kOffScratch == kOffBuf + size_t(kBufCap) * 8, "contiguous work area");
+static_assert(kBigWorkBytes <= size_t(kBufCap + kScratch) * 8, "kBig work area");
+static_assert(size_t(kBigCap) * 8 <= size_t(kBufCap + kScratch) * 8, "kBig band keys");
+
 struct RowShared {
   RowJob rowq[kStages];  // the row each ring phase starts (row = -1: no more rows)
+  BigShared big;
   int hist[256];
   SelShared sel;
   unsigned long long thmin[3];
@@ -178,7 +190,11 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = (a - (s - bb)) + (b - bb);
 }
 
-template <bool BF16>
+// BIG selects the rows a launch streams: false, every row other than the kBig
+// rows (hdr->n_active, from the front of the row list); true, the kBig rows
+// only (hdr->n_big, from the back).  The two are separate instantiations so
+// that each compiles only its own modes.
+template <bool BF16, bool BIG>
 __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_kernel(const Problem P) {
   using E = Elt<BF16>;
   constexpr int EPV = E::kPerVec;
@@ -211,10 +227,17 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     S.tmpcount = 0;
   }
   __syncthreads();
-  pdl_wait();     // the setup kernel's lists and header
-  pdl_trigger();  // the filter kernel may launch; it waits for this kernel
+  // the previous kernel: the setup kernel (its lists and header), or for the
+  // kBig rows the other row pass (which waited for the setup kernel)
+  pdl_wait();
+  pdl_trigger();  // the next kernel may launch; it waits for this one
 
-  const int n_active = w.hdr->n_active;
+  const int n_active = BIG ? w.hdr->n_big : w.hdr->n_active;
+  const int64_t last_row = P.Rt + P.Rd - 1;  // kBig row j is listed at last_row - j
+  auto listed = [&](int j) -> const RowJob& {
+    return BIG ? w.rowlist[last_row - j] : w.rowlist[j];
+  };
+  int* const claim_ctr = BIG ? &w.hdr->rp_next_big : &w.hdr->rp_next;
   const int64_t row_bytes = int64_t(P.V) * E::kSize;
   const int64_t bulk = row_bytes & ~int64_t(15);
   const int ntiles = int((bulk + kTileBytes - 1) / kTileBytes);
@@ -233,9 +256,8 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     // read it once the phase completes); a row without bulk tiles, and the
     // end of the list, take a phase of their own with no copy.  `issued`
     // counts phases.
-    const int claim_t = ntiles > 4 ? ntiles - 4 : 0;
     int j = blockIdx.x;
-    RowJob job = w.rowlist[min(j, max(n_active - 1, 0))];
+    RowJob job = listed(min(j, max(n_active - 1, 0)));
     for (uint32_t q = 0; !stop; ++q) {
       const bool end = j >= n_active;
       if (end) job.row = -1;
@@ -244,7 +266,11 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           row < P.Rt
               ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
               : static_cast<const char*>(P.draft) + (row - P.Rt) * P.d_stride * E::kSize;
-      const int nt = end ? 0 : ntiles;
+      // a kBig row is streamed kBigPasses times; its earlier streams keep the
+      // default L2 policy so that the later ones are served from L2
+      const int passes = BIG ? kBigPasses : 1;
+      const int nt = end ? 0 : ntiles * passes;
+      const int claim_t = nt > 4 ? nt - 4 : 0;
       int jn = n_active;
       for (int t = 0; t < (nt > 0 ? nt : 1); ++t) {
         if (!wait_or_abort(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
@@ -254,15 +280,20 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
           break;
         }
         if (t == 0) S.rowq[q % kStages] = job;
-        if (t == claim_t && !end) jn = int(gridDim.x) + atomicAdd(&w.hdr->rp_next, 1);
+        if (t == claim_t && !end) jn = int(gridDim.x) + atomicAdd(claim_ctr, 1);
         if (nt == 0) {
           mbar_arrive(full0 + 8u * stage);
         } else {
-          const int64_t rem = bulk - int64_t(t) * kTileBytes;
+          const int tt = passes == 1 ? t : t % ntiles;  // tile of the row
+          const int64_t rem = bulk - int64_t(tt) * kTileBytes;
           const uint32_t bytes = uint32_t(rem < kTileBytes ? rem : kTileBytes);
           mbar_arrive_expect_tx(full0 + 8u * stage, bytes);
-          bulk_load_hint(smem_addr(ring + size_t(stage) * kTileBytes),
-                         src + int64_t(t) * kTileBytes, bytes, full0 + 8u * stage, stream_pol);
+          if (t >= nt - ntiles)  // the row's last stream: read once more, never again
+            bulk_load_hint(smem_addr(ring + size_t(stage) * kTileBytes),
+                           src + int64_t(tt) * kTileBytes, bytes, full0 + 8u * stage, stream_pol);
+          else
+            bulk_load(smem_addr(ring + size_t(stage) * kTileBytes),
+                      src + int64_t(tt) * kTileBytes, bytes, full0 + 8u * stage);
         }
         ++issued;
         if (++stage == kStages) {
@@ -272,7 +303,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       }
       if (end) break;
       j = jn;
-      if (j < n_active) job = w.rowlist[j];
+      if (j < n_active) job = listed(j);
     }
     if (stop || *reinterpret_cast<volatile int*>(&S.cabort)) {
       // Let every copy this CTA issued land before the CTA may exit.
@@ -331,14 +362,19 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     const int64_t row = ent.row;
     const int b = ent.b;
     const int gx = ent.gx;
-    const int mode = ent.mode & 3;
+    const int mode = ent.mode & kModeMask;
     const float T = ent.T;
     const int Kreq = ent.K;
     const void* rowp =
         row < P.Rt ? static_cast<const char*>(P.target) + row * P.t_stride * E::kSize
                    : static_cast<const char*>(P.draft) + (row - P.Rt) * P.d_stride * E::kSize;
 
-    if (mode == kStats) {
+    if (BIG) {
+      // ---------------------------------------------- top-p alone / large top-k
+      const BigRing br{ring, full0, empty0, &stage, &phase, &S.cabort, &S.pabort, w.hdr};
+      big_row<E>(P, br, S.big, S.hist, &S.sel, smem + kOffBuf, ent, rowp, ntiles, last_nvec,
+                 tail_start, n_tail);
+    } else if (mode == kStats) {
       // ---------------------------------------------- online softmax sums
       const float c2 = __fdiv_rn(1.4426950408889634f, T);  // log2(e) / T
       float m = -INFINITY, s = 0.f, comp = 0.f;
@@ -1062,18 +1098,29 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
 
 size_t rowpass_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_rowpass(const Problem& P, bool bf16, int grid, cudaStream_t s) {
+cudaError_t launch_rowpass(const Problem& P, bool bf16, bool big, int grid, cudaStream_t s) {
   if (bf16)
-    return launch_after(rowpass_kernel<true>, grid, kRowpassThreads, kSmemBytes, s, P);
-  return launch_after(rowpass_kernel<false>, grid, kRowpassThreads, kSmemBytes, s, P);
+    return big ? launch_after(rowpass_kernel<true, true>, grid, kRowpassThreads, kSmemBytes, s, P)
+               : launch_after(rowpass_kernel<true, false>, grid, kRowpassThreads, kSmemBytes, s,
+                              P);
+  return big ? launch_after(rowpass_kernel<false, true>, grid, kRowpassThreads, kSmemBytes, s, P)
+             : launch_after(rowpass_kernel<false, false>, grid, kRowpassThreads, kSmemBytes, s, P);
 }
 
 cudaError_t rowpass_configure() {
-  cudaError_t e = cudaFuncSetAttribute(rowpass_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(rowpass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              int(kSmemBytes));
+  const int smem = int(kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(rowpass_kernel<true, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(rowpass_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(rowpass_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(rowpass_kernel<false, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  return e;
 }
 
 }  // namespace sv

@@ -54,6 +54,7 @@ struct ReqRows {
                // draft rows are not streamed (they get a defined record here)
   int tk;      // top-k
   float T;     // temperature
+  int big;     // the rows are kBig rows: listed from the end of the row list
 };
 
 // Writes the row list of the chunk's requests, one warp per request, so that
@@ -67,13 +68,14 @@ __device__ void fill_rows(const Problem& P, const ReqRows* rq, int base, int nb)
   constexpr int kW = kSetupThreads / 32;
   for (int r = blockIdx.x * kW + (threadIdx.x >> 5); r < nb; r += gridDim.x * kW) {
     const ReqRows q = rq[r];
+    const int last = int(P.Rt + P.Rd) - 1;
     for (int e = lane; e < q.active; e += 32) {
       const bool tgt = e <= q.k;
       const int i = tgt ? e : e - q.k - 1;
       const int row = tgt ? q.t0 + i : int(P.Rt) + q.d0 + i;
       const int gx = i < q.k ? P.draft_tokens[q.d0 + i] : -1;
-      const int mode = (i << 2) | (tgt ? (q.modes & 0xff) : ((q.modes >> 8) & 0xff));
-      int4* dst = reinterpret_cast<int4*>(w.rowlist + q.a0 + e);
+      const int mode = (i << kModeBits) | (tgt ? (q.modes & 0xff) : ((q.modes >> 8) & 0xff));
+      int4* dst = reinterpret_cast<int4*>(w.rowlist + (q.big ? last - (q.a0 + e) : q.a0 + e));
       dst[0] = make_int4(row, base + r, gx, mode);
       dst[1] = make_int4(__float_as_int(q.T), q.tk, 0, 0);
     }
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       w.hdr->n_decide = 0;
       w.hdr->n_draw = 0;
       w.hdr->rp_next = 0;
+      w.hdr->n_big = 0;
+      w.hdr->rp_next_big = 0;
     }
     s_bad = 0;
   }
@@ -164,7 +168,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
 
   // Pass 2: per-request validation, modes, the active row list and the
   // post-pass job lists (filtered requests; all others).
-  int carry_a = 0, carry_f = 0, carry_o = 0;
+  int carry_a = 0, carry_g = 0, carry_f = 0, carry_o = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int code = 0, active = 0, mode_t = kSkip, mode_d = kSkip, k = 0, t0 = 0, d0 = 0;
@@ -182,7 +186,6 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       if (!(T >= 0.0f) || isinf(T)) code = SV_ERR_DATA_TEMPERATURE;
       else if (!(tp > 0.0f && tp <= 1.0f)) code = SV_ERR_DATA_TOP_P;
       else if (tk < 0) code = SV_ERR_DATA_TOP_K;
-      else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
       else if (T > 0.0f && k > 0 && P.draft == nullptr) code = SV_ERR_DATA_NO_DRAFT;
       if (!code) {
         // no early exit: the (at most SV_MAX_K) loads are independent
@@ -202,22 +205,32 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
         mode_t = kArgmax;
         active = k + 1;
       } else if (code == 0) {
-        mode_t = mode_d = filtered ? kTopk : kStats;
+        // a small top-k takes the candidate path; top-p alone and larger
+        // top-k take the threshold path
+        mode_t = mode_d = !filtered ? kStats : (topk_on && tk <= SV_TOPK_MAX ? kTopk : kBig);
         active = 2 * k + 1;
       }
     }
     const bool filt = !code && mode_t == kTopk;
-    // active rows (low half); filtered requests and the others (high half,
-    // 16 bits each: a chunk holds at most kSetupThreads requests)
+    const bool big = !code && mode_t == kBig;
+    // four counters in one word: other active rows (bits 0-19), kBig rows
+    // (20-39), filtered requests (40-51) and the other requests (52-63); a
+    // chunk holds at most kSetupThreads requests of at most 2 SV_MAX_K + 1
+    // rows each
+    static_assert(kSetupThreads * (2 * SV_MAX_K + 1) < (1 << 20) && kSetupThreads < (1 << 12),
+                  "setup scan fields");
     unsigned long long tot;
-    const uint32_t fo = b < P.B ? (filt ? 1u : 1u << 16) : 0u;
-    const unsigned long long ex = block_exclusive_scan(pack2(uint32_t(active), fo), &tot);
-    const int a0 = carry_a + int(uint32_t(ex));
-    const int f0 = carry_f + int((ex >> 32) & 0xffffu);
-    const int o0 = carry_o + int(ex >> 48);
-    carry_a += int(uint32_t(tot));
-    carry_f += int((tot >> 32) & 0xffffu);
-    carry_o += int(tot >> 48);
+    const unsigned long long fo =
+        b < P.B ? (filt ? 1ull << 40 : 1ull << 52) : 0ull;
+    const unsigned long long ex = block_exclusive_scan(
+        (big ? uint64_t(active) << 20 : uint64_t(active)) | fo, &tot);
+    const int a0 = big ? carry_g + int((ex >> 20) & 0xfffffu) : carry_a + int(ex & 0xfffffu);
+    const int f0 = carry_f + int((ex >> 40) & 0xfffu);
+    const int o0 = carry_o + int(ex >> 52);
+    carry_a += int(tot & 0xfffffu);
+    carry_g += int((tot >> 20) & 0xfffffu);
+    carry_f += int((tot >> 40) & 0xfffu);
+    carry_o += int(tot >> 52);
     if (b < P.B && lead) {
       w.seg_cnt[b] = 0;
       if (filt)
@@ -227,13 +240,15 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
     }
     s_req[threadIdx.x] =
         ReqRows{a0, t0, d0, k, b < P.B ? active : 0,
-                mode_t | (mode_d << 8) | (b < P.B && mode_d == kSkip ? 1 << 16 : 0), tk, T};
+                mode_t | (mode_d << 8) | (b < P.B && mode_d == kSkip ? 1 << 16 : 0), tk, T,
+                big ? 1 : 0};
     __syncthreads();
     fill_rows(P, s_req, base, min(kSetupThreads, P.B - base));
     __syncthreads();  // s_req is rewritten by the next chunk
   }
   if (threadIdx.x == 0 && lead) {
     w.hdr->n_active = carry_a;
+    w.hdr->n_big = carry_g;
     w.hdr->n_filtered = carry_f;
     w.hdr->n_decide = carry_o;
   }
@@ -248,9 +263,10 @@ __device__ void fill_sample_rows(const Problem& P, const ReqRows* rq, int base, 
   constexpr int kW = kSetupThreads / 32;
   for (int r = blockIdx.x * kW + (threadIdx.x >> 5); r < nb; r += gridDim.x * kW) {
     const ReqRows q = rq[r];
+    const int last = int(P.Rt) - 1;
     for (int i = lane; i < q.active; i += 32) {
-      int4* dst = reinterpret_cast<int4*>(w.rowlist + q.a0 + i);
-      dst[0] = make_int4(q.t0 + i, base + r, -1, (i << 2) | q.modes);
+      int4* dst = reinterpret_cast<int4*>(w.rowlist + (q.big ? last - (q.a0 + i) : q.a0 + i));
+      dst[0] = make_int4(q.t0 + i, base + r, -1, (i << kModeBits) | q.modes);
       dst[1] = make_int4(__float_as_int(q.T), q.tk, 0, 0);
     }
   }
@@ -282,6 +298,8 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     w.hdr->n_draw = 0;
     w.hdr->next_row = 0;
     w.hdr->rp_next = 0;
+    w.hdr->n_big = 0;
+    w.hdr->rp_next_big = 0;
   }
   if (threadIdx.x == 0) s_bad = 0;
   // every row may queue a draw: their segment counters start at zero
@@ -326,7 +344,7 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
   if (s_bad) return;
 
   // Pass 2: per-request validation, modes and the row list.
-  int carry_a = 0;
+  int carry_a = 0, carry_g = 0;
   for (int base = 0; base < P.B; base += kSetupThreads) {
     const int b = base + threadIdx.x;
     int code = 0, active = 0, mode = kSkip, k = 0, d0 = 0, tk = 0;
@@ -342,7 +360,6 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
       if (!(T >= 0.0f) || isinf(T)) code = SV_ERR_DATA_TEMPERATURE;
       else if (!(tp > 0.0f && tp <= 1.0f)) code = SV_ERR_DATA_TOP_P;
       else if (tk < 0) code = SV_ERR_DATA_TOP_K;
-      else if (filtered && (!topk_on || tk > SV_TOPK_MAX)) code = SV_ERR_DATA_TOP_K;
       if (code && lead) {
         w.req_flag[b] = code;
         record_error(w.hdr, code, b, -1);
@@ -354,20 +371,29 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
         w.req_flag[b] = 0;
       }
       if (!code) {
-        mode = T == 0.0f ? kArgmax : (filtered ? kTopk : kStats);
+        mode = T == 0.0f ? kArgmax
+                         : (!filtered ? kStats : (topk_on && tk <= SV_TOPK_MAX ? kTopk : kBig));
         active = k;
       }
     }
+    // other rows (low half), kBig rows (high half)
+    const bool big = mode == kBig;
     unsigned long long tot;
-    const int a0 = carry_a + int(uint32_t(block_exclusive_scan(uint32_t(active), &tot)));
+    const unsigned long long ex =
+        block_exclusive_scan(big ? pack2(0u, uint32_t(active)) : pack2(uint32_t(active), 0u), &tot);
+    const int a0 = big ? carry_g + int(ex >> 32) : carry_a + int(uint32_t(ex));
     carry_a += int(uint32_t(tot));
-    // fill_sample_rows reads a0, t0 (the first drafter row), active, modes, tk, T
-    s_req[threadIdx.x] = ReqRows{a0, d0, 0, k, active, mode, tk, T};
+    carry_g += int(tot >> 32);
+    // fill_sample_rows reads a0, t0 (the first drafter row), active, modes, tk, T, big
+    s_req[threadIdx.x] = ReqRows{a0, d0, 0, k, active, mode, tk, T, big ? 1 : 0};
     __syncthreads();
     fill_sample_rows(P, s_req, base, min(kSetupThreads, P.B - base));
     __syncthreads();  // s_req is rewritten by the next chunk
   }
-  if (threadIdx.x == 0 && lead) w.hdr->n_active = carry_a;
+  if (threadIdx.x == 0 && lead) {
+    w.hdr->n_active = carry_a;
+    w.hdr->n_big = carry_g;
+  }
 }
 
 }  // namespace

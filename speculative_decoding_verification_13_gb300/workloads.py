@@ -160,7 +160,10 @@ def _sample_draft_tokens(draft, temps, top_k, top_p, owner, g, chunk):
                 order = torch.argsort(z, dim=1, descending=True, stable=True)
                 ps = pr.gather(1, order)
                 before = torch.cumsum(ps, dim=1) - ps
-                keep = before < tp[:, None]
+                # the first token always stays (also for an invalid top_p of a
+                # data-error test, so that the draw is defined)
+                first = torch.arange(V, device=x.device)[None] == 0
+                keep = (before < tp[:, None]) | first
                 ps = torch.where(keep, ps, torch.zeros_like(ps))
                 pr = torch.zeros_like(pr).scatter_(1, order, ps)
                 del order, ps, before, keep
@@ -174,7 +177,7 @@ def _sample_draft_tokens(draft, temps, top_k, top_p, owner, g, chunk):
             in_k = (col < tk[:, None]) & on[:, None] | (col == 0) & ~on[:, None]
             pr = torch.softmax(vals.masked_fill(~in_k, float("-inf")), dim=1)
             before = torch.cumsum(pr, dim=1) - pr
-            keep = (before < tp[:, None]) & in_k
+            keep = ((before < tp[:, None]) | (col == 0)) & in_k
             pr = torch.where(keep, pr, torch.zeros_like(pr))
             pick = torch.multinomial(pr, 1, generator=g).squeeze(1)
             samp_k = idx.gather(1, pick[:, None]).squeeze(1)

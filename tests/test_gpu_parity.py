@@ -287,11 +287,8 @@ def test_data_errors_are_reported_per_request():
     _expect(b, 17, {2})
     b = custom([2, 3, 1], [1.0, 1.0, 0.0], 500, torch.float32, top_p=[1.0, 0.0, 1.0])
     _expect(b, 18, {1})
-    b = custom([2, 3, 1], [1.0, 1.0, 0.0], 500, torch.float32, top_k=[0, 300, 0])
+    b = custom([2, 3, 1], [1.0, 1.0, 0.0], 500, torch.float32, top_k=[0, -3, 0])
     _expect(b, 19, {1})
-    b = custom([2, 3, 1], [1.0, 1.0, 0.0], 500, torch.float32, top_k=[0, 0, 0],
-               top_p=[0.5, 1.0, 1.0])
-    _expect(b, 19, {0})      # top-p without top-k is not supported by this build
     b = custom([2, 3, 1], [1.0, 1.0, 0.0], 500, torch.float32)
     b.draft[:] = float("-inf")
     _expect(b, 22, {0, 1})
