@@ -377,34 +377,81 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     } else if (mode == kStats) {
       // ---------------------------------------------- online softmax sums
       const float c2 = __fdiv_rn(1.4426950408889634f, T);  // log2(e) / T
-      float m = -INFINITY, s = 0.f, comp = 0.f;
+      float m = -INFINITY, mc2 = 0.f, s = 0.f, comp = 0.f;
+      bool nan_seen = false;
+      // 2^((x - m) log2(e) / T).  bf16 rows fold the shift into one FMA with
+      // m log2(e) / T rounded once (a few ulp of it, common to every term
+      // taken at the same m: far inside the bf16 probability tolerance); f32
+      // rows keep x - m exact.
+      auto term = [&](float x) -> float {
+        return ex2_approx(BF16 ? fmaf(x, c2, -mc2) : (x - m) * c2);
+      };
+      auto raise = [&](float vm) {  // a new running maximum vm > m
+        if (m != -INFINITY) {
+          const float f = ex2_approx((m - vm) * c2);
+          s *= f;
+          comp *= f;
+        }
+        m = vm;
+        mc2 = vm * c2;
+      };
+      auto add = [&](float acc) {  // Kahan-compensated running sum
+        const float y = acc - comp;
+        const float t2 = s + y;
+        comp = (t2 - s) - y;
+        s = t2;
+      };
+      // n elements (a partial tile, the tail); the maximum propagates NaN
       auto consume = [&](const float* x, int n) {
         float vm = x[0];
-        for (int e = 1; e < n; ++e) vm = fmaxf(vm, x[e]);
-        if (vm > m) {
-          if (m != -INFINITY) {
-            const float f = ex2_approx((m - vm) * c2);
-            s *= f;
-            comp *= f;
-          }
-          m = vm;
-        }
+        for (int e = 1; e < n; ++e) vm = fmax_nan(vm, x[e]);
+        nan_seen |= vm != vm;
+        if (vm > m) raise(vm);
         if (m != -INFINITY) {
           float acc = 0.f;
-          for (int e = 0; e < n; ++e) acc += ex2_approx((x[e] - m) * c2);
-          const float y = acc - comp;  // Kahan-compensated running sum
-          const float t2 = s + y;
-          comp = (t2 - s) - y;
-          s = t2;
+          for (int e = 0; e < n; ++e) acc += term(x[e]);
+          add(acc);
         }
       };
+      constexpr int VPT = (kTileBytes / 16 + kConsumers - 1) / kConsumers;
       for (int t = 0; t < ntiles; ++t) {
         const uint4* tile = acquire();
         const int nvec = tile_vectors(t);
-        for (int v = ctid; v < nvec; v += kConsumers) {
-          float x[EPV];
-          E::decode(tile[v], x);
-          consume(x, EPV);
+        if (nvec == kTileBytes / 16) {
+          // a full tile: two vectors per step, their 2 EPV terms summed as a
+          // tree (independent exponentials, short dependency chains)
+#pragma unroll
+          for (int i = 0; i < VPT; i += 2) {
+            const uint4 qa = tile[ctid + i * kConsumers], qb = tile[ctid + (i + 1) * kConsumers];
+            float x[2 * EPV];
+            E::decode(qa, x);
+            E::decode(qb, x + EPV);
+            float vm;
+            if constexpr (BF16) {
+              const uint32_t pm = bmax2_nan(E::pmax(qa), E::pmax(qb));
+              vm = fmax_nan(bf16_lo(pm), bf16_hi(pm));
+            } else {
+              vm = fmax_nan(E::vmax(qa), E::vmax(qb));
+            }
+            nan_seen |= vm != vm;
+            if (vm > m) raise(vm);
+            if (m != -INFINITY) {
+              float e[2 * EPV];
+#pragma unroll
+              for (int k = 0; k < 2 * EPV; ++k) e[k] = term(x[k]);
+#pragma unroll
+              for (int w2 = 1; w2 < 2 * EPV; w2 <<= 1)
+#pragma unroll
+                for (int k = 0; k + w2 < 2 * EPV; k += 2 * w2) e[k] += e[k + w2];
+              add(e[0]);
+            }
+          }
+        } else {
+          for (int v = ctid; v < nvec; v += kConsumers) {
+            float x[EPV];
+            E::decode(tile[v], x);
+            consume(x, EPV);
+          }
         }
         release();
       }
@@ -412,6 +459,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
         const float x = E::scalar(rowp, tail_start + ctid);
         consume(&x, 1);
       }
+      if (nan_seen) s = __int_as_float(0x7fc00000);  // a NaN logit: the row is bad
       // block max, then TwoSum-reduced sum rescaled to it
       float M = m;
 #pragma unroll
