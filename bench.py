@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "spec-verify rows/s and HBM GB/s vs ~8 TB/s peak at B=256,k=15,V=151936 bf16"
 UNIT = "rows/s"
-EVENT_EVERY = 8  # timed steps per row-pass event pair
+EVENT_EVERY = 8  # draft-sampler line: timed steps per row-pass event pair
+ROWPASS_STEPS = 32  # verification line: steps timed for the row passes alone, after the K steps
 L2_BYTES = 129 * 1000 * 1000
 FLUSH_BYTES = 512 << 20  # written between steps when the inputs fit in L2
 
@@ -790,14 +791,11 @@ def main():
     if code != 0:
         raise RuntimeError(f"device data error {code} during warm-up")
 
-    # timed region: K steps.  The row pass is bracketed by CUDA events on every
-    # EVENT_EVERY-th step: an event recorded between two kernels ends the
-    # overlap of one kernel's launch with the previous one's tail (about 8 us a
-    # step on the bench workload), so bracketing every step would charge that
-    # measurement cost to the step time.  With an L2 flush between steps each
-    # step is bracketed by its own events (the flush is not timed).
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           if i % EVENT_EVERY == 0 else None for i in range(args.steps)]
+    # timed region: K steps, no events between the kernels of a step (an
+    # event recorded between two kernels ends the overlap of one kernel's
+    # launch with the previous one's tail, about 8 us a step on the bench
+    # workload).  With an L2 flush between steps each step is bracketed by its
+    # own events (the flush is not timed).
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     steps_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)] if flush else None
@@ -809,7 +807,7 @@ def main():
         if flush:
             scratch.fill_(i & 255)
             steps_ev[i][0].record(stream)
-        call(evs[i])
+        call()
         if flush:
             steps_ev[i][1].record(stream)
     end.record(stream)
@@ -820,7 +818,16 @@ def main():
         step_ms = sum(a.elapsed_time(b) for a, b in steps_ev) / args.steps
     else:
         step_ms = start.elapsed_time(end) / args.steps
-    timed = [e for e in evs if e is not None]
+    # the streaming kernels alone: ROWPASS_STEPS more steps, each with events
+    # recorded by the library right before and after its row passes
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(ROWPASS_STEPS)]
+    for i in range(ROWPASS_STEPS):
+        if flush:
+            scratch.fill_(i & 255)
+        call(evs[i])
+    torch.cuda.synchronize(dev)
+    timed = evs
     rowpass_ms = sum(a.elapsed_time(b) for a, b in timed) / len(timed)
     clk = clocks.stop() if clocks else None
 

@@ -76,7 +76,8 @@ extern "C" {
 #define SV_ERR_DATA_LOGIT 22        /* NaN or +inf logit, or (sampling) a row    */
                                     /* with no finite logit                      */
 #define SV_ERR_DATA_NO_DRAFT 23     /* temperature > 0 but draft logits absent   */
-#define SV_ERR_TIMEOUT 24           /* an internal bounded wait expired          */
+#define SV_ERR_TIMEOUT 24           /* an internal bounded wait expired (each    */
+                                    /* wait gives up after 100 ms of GPU time)   */
 #define SV_ERR_INTERNAL 25          /* an internal capacity invariant failed     */
 #define SV_ERR_DATA_ACCEPT 26       /* KV commit: accept length above k_b         */
 #define SV_ERR_DATA_PAGE 27         /* KV commit: a destination page missing from */
@@ -113,6 +114,12 @@ typedef struct {
    * the row-streaming kernel (profiling); NULL to skip. */
   void* event_rowpass_begin;
   void* event_rowpass_end;
+  /* Test of the timeout path (0 in normal use): nonzero makes one bounded
+   * wait of the row pass expire, as a stalled copy's would; the request of
+   * the first listed row then fails with SV_ERR_TIMEOUT and every other
+   * request is verified as usual.  spec_verify only. */
+  int32_t test_expire_wait;
+  int32_t reserved;
 } sv_options;
 
 /* Bytes of device workspace spec_verify needs for this shape; 0 on bad

@@ -65,7 +65,8 @@ class _Logits(ctypes.Structure):
 
 class _Options(ctypes.Structure):
     _fields_ = [("out_pq", ctypes.c_void_p), ("event_rowpass_begin", ctypes.c_void_p),
-                ("event_rowpass_end", ctypes.c_void_p)]
+                ("event_rowpass_end", ctypes.c_void_p), ("test_expire_wait", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class _KvCache(ctypes.Structure):
@@ -242,7 +243,10 @@ class Verifier:
 
     def __call__(self, target, draft, draft_tokens, k_per_req, temperature, uniforms,
                  top_k=None, top_p=None, *, out_accept_len=None, out_tokens=None,
-                 out_pq=None, stream=None, rowpass_events=None):
+                 out_pq=None, stream=None, rowpass_events=None, test_expire_wait=False):
+        """test_expire_wait: test of the timeout path only (one bounded wait of
+        the row pass expires; the first listed row's request fails with
+        SV_ERR_TIMEOUT)."""
         lib = load_library()
         B = int(k_per_req.shape[0])
         _check(k_per_req, "k_per_req", torch.int32)
@@ -271,10 +275,10 @@ class Verifier:
         with torch.cuda.device(target.device):
             ws = self._workspace(B, Rt, Rd)
             opts = None
-            if out_pq is not None or rowpass_events is not None:
+            if out_pq is not None or rowpass_events is not None or test_expire_wait:
                 ev0, ev1 = rowpass_events if rowpass_events is not None else (None, None)
                 opts = _Options(_ptr(out_pq), _event_handle(ev0, stream),
-                                _event_handle(ev1, stream))
+                                _event_handle(ev1, stream), 1 if test_expire_wait else 0, 0)
             rc = lib.spec_verify(ctypes.byref(td), ctypes.byref(dd), _ptr(draft_tokens),
                                  _ptr(k_per_req), _ptr(temperature), _ptr(top_k), _ptr(top_p),
                                  _ptr(uniforms), _ptr(out_accept_len), _ptr(out_tokens),
@@ -332,7 +336,7 @@ class DraftSampler:
         opts = None
         if rowpass_events is not None:
             ev0, ev1 = rowpass_events
-            opts = _Options(None, _event_handle(ev0, stream), _event_handle(ev1, stream))
+            opts = _Options(None, _event_handle(ev0, stream), _event_handle(ev1, stream), 0, 0)
         rc = lib.spec_draft_sample(ctypes.byref(xd), _ptr(k_per_req), _ptr(temperature),
                                    _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
                                    _ptr(out_q), _stream_handle(stream), B, _ptr(ws), ws.numel(),
@@ -551,7 +555,7 @@ def verify_noalloc(target, draft, draft_tokens, k_per_req, temperature, uniforms
         dd.dtype = td.dtype
     _check_verify_args(target, draft, draft_tokens, k_per_req, temperature, uniforms, top_k,
                        top_p, out_accept_len, out_tokens, out_pq, int(td.rows), int(dd.rows))
-    opts = _Options(_ptr(out_pq), None, None) if out_pq is not None else None
+    opts = _Options(_ptr(out_pq), None, None, 0, 0) if out_pq is not None else None
     # the library looks up the buffer of the current device: make it the
     # logits' device
     with torch.cuda.device(target.device):

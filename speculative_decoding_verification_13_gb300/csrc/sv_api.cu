@@ -133,6 +133,7 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   P.out_pq = options ? options->out_pq : nullptr;
   P.out_q = nullptr;
   P.n_seg = 1;
+  P.test_expire = options ? options->test_expire_wait : 0;
   P.ws = ws_bind(workspace, L);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -217,6 +218,7 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   P.out_tokens = out_tokens;
   P.out_pq = nullptr;
   P.out_q = out_q;
+  P.test_expire = 0;
   P.ws = ws_bind(workspace, L);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -84,18 +84,7 @@ struct BigRing {
 
 __device__ __forceinline__ const uint4* big_acquire(const BigRing& r) {
   const uint32_t bar = r.full0 + 8u * *r.stage;
-  bool ok = false;
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait(bar, *r.phase)) {
-      ok = true;
-      break;
-    }
-    if ((it & 255u) == 255u && (*reinterpret_cast<volatile int*>(r.cabort) ||
-                                *reinterpret_cast<volatile int*>(r.pabort)))
-      break;
-    __nanosleep(16);
-  }
-  if (!ok) {
+  if (!mbar_wait_for(bar, *r.phase, kWaitNs, r.cabort, r.pabort, 16)) {
     *reinterpret_cast<volatile int*>(r.cabort) = 1;
     record_error(r.hdr, SV_ERR_TIMEOUT, -1, -1);
   }

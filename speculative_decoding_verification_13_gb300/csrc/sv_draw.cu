@@ -132,14 +132,7 @@ struct DrawPassShared {
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const int* f1,
                                          const int* f2, uint32_t sleep_ns) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u &&
-        (*reinterpret_cast<const volatile int*>(f1) || *reinterpret_cast<const volatile int*>(f2)))
-      return false;
-    __nanosleep(sleep_ns);
-  }
-  return false;
+  return mbar_wait_for(bar, parity, kWaitNs, f1, f2, sleep_ns);
 }
 
 __device__ __forceinline__ void draw_sync() {
@@ -253,8 +246,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
       const long long first = issued > kDStages ? issued - kDStages : 0;
       for (long long g = first; g < issued; ++g) {
         const uint32_t st = uint32_t(g % kDStages), ph = uint32_t((g / kDStages) & 1);
-        for (uint32_t it = 0; it < kWaitLimit; ++it)
-          if (mbar_try_wait(full0 + 8u * st, ph)) break;
+        mbar_wait_for(full0 + 8u * st, ph);
       }
     }
     return;

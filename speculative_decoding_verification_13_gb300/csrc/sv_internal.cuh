@@ -24,7 +24,9 @@ constexpr int kRawCap = 1024;                            // top-k survivors kept
 constexpr int kScratch = 1024;                           // selection scratch entries
 constexpr int kStage = 64;                               // staged flagged vectors per warp
 constexpr int kTopkMax = SV_TOPK_MAX;
-constexpr uint32_t kWaitLimit = 1u << 24;                // bounded mbarrier waits
+constexpr uint64_t kWaitNs = 100ull * 1000 * 1000;       // a wait gives up after 100 ms
+constexpr uint32_t kWaitPolls = 1u << 28;                // ... or after this many polls
+constexpr uint64_t kTestWaitNs = 1000ull * 1000;         // the expiring test wait: 1 ms
 constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
 
 // Row modes chosen per request by the setup kernel.  kTopk: a filtered row
@@ -170,6 +172,7 @@ struct Problem {
   int32_t V;
   int32_t B;
   int32_t n_seg;                // draw-pass segments per queued draw (1..kMaxSeg)
+  int32_t test_expire;          // test only: one bounded wait of the row pass expires
   const int32_t* draft_tokens;
   const int32_t* k_per_req;
   const float* temperature;
@@ -279,11 +282,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait: false when the limit ran out (the caller records SV_ERR_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
+// Nanoseconds of the GPU's global timer (wall-clock time).
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: true once the phase completes; false
+// after limit_ns of GPU wall-clock time without completion, after kWaitPolls
+// polls, or as soon as one of the optional abort flags is set (both checked
+// every 256 polls).  The caller records SV_ERR_TIMEOUT.  sleep_ns: back-off
+// between polls, so that a waiting warp leaves the issue slots to the warps
+// that work.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity,
+                                              uint64_t limit_ns = kWaitNs,
+                                              const int* f1 = nullptr, const int* f2 = nullptr,
+                                              uint32_t sleep_ns = 0) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1; it < kWaitPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0u) {
+      if (f1 && *reinterpret_cast<const volatile int*>(f1)) return false;
+      if (f2 && *reinterpret_cast<const volatile int*>(f2)) return false;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+    if (sleep_ns) __nanosleep(sleep_ns);
+  }
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity);
 }
 
 // One bulk global -> shared copy completing on an mbarrier (TMA, non-tensor form).

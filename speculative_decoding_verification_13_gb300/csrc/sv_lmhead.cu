@@ -104,11 +104,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // Bounded wait on an mbarrier phase; false (and the CTA's abort flag set) on expiry.
 __device__ __forceinline__ bool lm_wait(uint32_t bar, uint32_t parity, int* abort_flag,
                                         uint32_t sleep_ns) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u && *reinterpret_cast<volatile int*>(abort_flag)) return false;
-    __nanosleep(sleep_ns);
-  }
+  if (mbar_wait_for(bar, parity, kWaitNs, abort_flag, nullptr, sleep_ns)) return true;
   *reinterpret_cast<volatile int*>(abort_flag) = 1;
   return false;
 }
@@ -181,8 +177,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const long long first = issued > kLmStages ? issued - kLmStages : 0;
       for (long long g = first; g < issued; ++g) {
         const uint32_t st = uint32_t(g % kLmStages), ph = uint32_t((g / kLmStages) & 1);
-        for (uint32_t it = 0; it < kWaitLimit; ++it)
-          if (mbar_try_wait(full0 + 8u * st, ph)) break;
+        mbar_wait_for(full0 + 8u * st, ph);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -228,8 +223,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       record_error(A.hdr, SV_ERR_TIMEOUT, -1, -1);
       // every MMA issued must finish before TMEM is freed: commit once more and wait
       umma_commit(afull0 + 8u * ab);
-      for (uint32_t it = 0; it < kWaitLimit; ++it)
-        if (mbar_try_wait(afull0 + 8u * ab, aphase)) break;
+      mbar_wait_for(afull0 + 8u * ab, aphase);
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue

@@ -58,6 +58,7 @@ static_assert(size_t(kBigCap) * 8 <= size_t(kBufCap + kScratch) * 8, "kBig band 
 
 struct RowShared {
   RowJob rowq[kStages];  // the row each ring phase starts (row = -1: no more rows)
+  unsigned long long test_bar_word;  // an mbarrier nothing arrives on (timeout test)
   BigShared big;
   int hist[256];
   SelShared sel;
@@ -143,14 +144,7 @@ struct Elt<false> {
 // does not take issue slots from the warps that do the work.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const int* f1,
                                               const int* f2, uint32_t sleep_ns) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 255u &&
-        (*reinterpret_cast<const volatile int*>(f1) || *reinterpret_cast<const volatile int*>(f2)))
-      return false;
-    __nanosleep(sleep_ns);
-  }
-  return false;
+  return mbar_wait_for(bar, parity, kWaitNs, f1, f2, sleep_ns);
 }
 
 // A bf16 value d below v (v itself a bf16 value), in both halves of a
@@ -206,6 +200,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
   uint64_t* xchg = reinterpret_cast<uint64_t*>(smem + kOffXchg);
   const uint32_t full0 = smem_addr(smem + kOffBars);
   const uint32_t empty0 = full0 + 8u * kStages;
+  const uint32_t test_bar = smem_addr(&S.test_bar_word);
   const Ws& w = P.ws;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -214,6 +209,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       mbar_init(full0 + 8u * s, 1);
       mbar_init(empty0 + 8u * s, kConsumerWarps);
     }
+    mbar_init(test_bar, 1);  // never arrived on (the timeout test)
     fence_mbar_init();
     S.cabort = 0;
     S.pabort = 0;
@@ -310,8 +306,7 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
       const long long first = issued > kStages ? issued - kStages : 0;
       for (long long g = first; g < issued; ++g) {
         const uint32_t st = uint32_t(g % kStages), ph = uint32_t((g / kStages) & 1);
-        for (uint32_t it = 0; it < kWaitLimit; ++it)
-          if (mbar_try_wait(full0 + 8u * st, ph)) break;
+        mbar_wait_for(full0 + 8u * st, ph);
       }
     }
     return;
@@ -358,6 +353,18 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     if (ab0) break;
     const RowJob ent = S.rowq[q % kStages];
     if (ent.row < 0) break;  // no more rows
+    if (P.test_expire && !BIG && blockIdx.x == 0 && q == 0) {
+      // Test of the timeout path: a bounded wait on a barrier nothing
+      // arrives on expires as a stalled copy's would.  The row's request
+      // fails with SV_ERR_TIMEOUT, this CTA stops; its producer sees the
+      // abort, lets the copies it issued land and exits.
+      if (!mbar_wait_for(test_bar, 0u, kTestWaitNs)) {
+        *reinterpret_cast<volatile int*>(&S.cabort) = 1;
+        if (ctid == 0) flag_request(w, ent.b, SV_ERR_TIMEOUT, ent.row);
+      }
+      consumer_sync();
+      break;
+    }
     if (ntiles == 0) release();  // a phase without a copy
     const int64_t row = ent.row;
     const int b = ent.b;
