@@ -318,6 +318,32 @@ int spec_lmhead_stats(const void* hidden, const void* unembed, int32_t rows, int
                       float* out_max, double* out_sum, int32_t* out_argmax, float* out_token,
                       void* stream, void* workspace, size_t workspace_bytes);
 
+/* ---- greedy verification from the target rows' argmax ----------------------
+ * At temperature 0 verification needs of each target row only its argmax
+ * (lowest index on ties): the longest prefix of drafts equal to it is accepted
+ * and the argmax at the first disagreement, or after a full acceptance, is
+ * emitted ("DFlash" §4 step 5; "Speculative decoding and multi-token
+ * prediction", "Draft and verify", step Three).  Fed by spec_lmhead_stats'
+ * out_argmax, a greedy request never needs its logits in memory.  Same row
+ * layout as spec_verify:
+ *   target_argmax  [R_t] int32, the argmax of target row t_off[b] + i
+ *   draft_tokens   [R_d] int32 (R_d = R_t - B)    k_per_req [B] int32
+ *   out_accept_len [B] int32 (L, or -1)           out_tokens [R_t] int32
+ *   vocab          V: tokens and argmax values must lie in [0, V)
+ *   workspace      >= spec_verify_greedy_workspace_size() bytes, 256-byte
+ *                  aligned; spec_verify_get_error reads its error record
+ * A k outside [0, SV_MAX_K] or sum(k + 1) != R_t fails the whole batch (all
+ * outputs -1, SV_ERR_DATA_K / SV_ERR_DATA_ROWS); a token or argmax outside
+ * [0, V) fails its request (SV_ERR_DATA_TOKEN).  Device pointers owned by the
+ * caller; asynchronous on `stream`.  Returns SV_OK once enqueued. */
+size_t spec_verify_greedy_workspace_size(void);
+
+int spec_verify_greedy_from_argmax(const int32_t* target_argmax, const int32_t* draft_tokens,
+                                   const int32_t* k_per_req, int32_t* out_accept_len,
+                                   int32_t* out_tokens, void* stream, int32_t batch,
+                                   int64_t target_rows, int32_t vocab, void* workspace,
+                                   size_t workspace_bytes);
+
 /* ---- adaptive speculation length -------------------------------------------
  * "Speculative decoding and multi-token prediction", section "Acceptance rate
  * is the whole economics": a drafted position beyond k is worth alpha^k tokens

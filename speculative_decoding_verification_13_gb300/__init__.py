@@ -29,7 +29,7 @@ __all__ = ["verify", "Verifier", "workspace_size", "get_error", "dump_rows", "st
            "library_path", "SpecVerifyError", "SV_TOPK_MAX", "SV_MAX_K", "verify_noalloc",
            "noalloc_scratch", "SV_NOALLOC_SCRATCH_BYTES", "DraftSampler", "draft_sample", "kv_commit",
            "kv_commit_error", "lmhead_stats", "lmhead_stats_error",
-           "adapt_k"]
+           "adapt_k", "verify_greedy_from_argmax", "verify_greedy_error"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libspecverify.so")
@@ -351,6 +351,59 @@ class DraftSampler:
 
 _default = {}
 _default_sampler = {}
+
+
+_greedy_ws = {}
+
+
+def verify_greedy_from_argmax(target_argmax, draft_tokens, k_per_req, vocab, *,
+                              out_accept_len=None, out_tokens=None, stream=None):
+    """Greedy verification from each target row's argmax (e.g. the out_argmax
+    of :func:`lmhead_stats`), so that the logits need not exist.  Returns
+    ``(accept_len [B] int32, tokens [R_t] int32)`` on the device."""
+    lib = load_library()
+    f = lib.spec_verify_greedy_from_argmax
+    if f.argtypes is None:
+        P = ctypes.c_void_p
+        f.restype = ctypes.c_int
+        f.argtypes = [P, P, P, P, P, P, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, P,
+                      ctypes.c_size_t]
+        lib.spec_verify_greedy_workspace_size.restype = ctypes.c_size_t
+        lib.spec_verify_greedy_workspace_size.argtypes = []
+    _check(target_argmax, "target_argmax", torch.int32)
+    _check(draft_tokens, "draft_tokens", torch.int32)
+    _check(k_per_req, "k_per_req", torch.int32)
+    B, Rt = int(k_per_req.numel()), int(target_argmax.numel())
+    dev = target_argmax.device
+    for t, n, name in ((draft_tokens, Rt - B, "draft_tokens"), (k_per_req, B, "k_per_req")):
+        if t.device != dev or t.numel() < n:
+            raise ValueError(f"{name} must be on {dev} with at least {n} elements")
+    if out_accept_len is None:
+        out_accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty(Rt, dtype=torch.int32, device=dev)
+    _check(out_accept_len, "out_accept_len", torch.int32)
+    _check(out_tokens, "out_tokens", torch.int32)
+    if out_accept_len.numel() < B or out_tokens.numel() < Rt:
+        raise ValueError("output tensors are too short")
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    need = int(lib.spec_verify_greedy_workspace_size())
+    ws = _greedy_ws.get(key)
+    if ws is None or ws.numel() < need:
+        ws = _greedy_ws[key] = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        rc = f(_ptr(target_argmax), _ptr(draft_tokens), _ptr(k_per_req), _ptr(out_accept_len),
+               _ptr(out_tokens), _stream_handle(stream), B, Rt, int(vocab), _ptr(ws), ws.numel())
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_greedy_from_argmax")
+    return out_accept_len, out_tokens
+
+
+def verify_greedy_error(stream=None, device=None):
+    """First data error of the last verify_greedy_from_argmax on this device."""
+    d = torch.device(device or "cuda")
+    return get_error(_greedy_ws[d.index if d.index is not None else torch.cuda.current_device()],
+                     stream)
 
 
 def adapt_k(accept_len, k_used, succ, fail, decay=0.9, c=0.1, k_min=1, k_max=16,

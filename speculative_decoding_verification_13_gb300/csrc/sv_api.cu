@@ -321,6 +321,27 @@ int spec_adapt_k(const int32_t* accept_len, const int32_t* k_used, double* succ,
              : SV_ERR_CUDA;
 }
 
+size_t spec_verify_greedy_workspace_size(void) { return align256(sizeof(WsHeader)); }
+
+int spec_verify_greedy_from_argmax(const int32_t* target_argmax, const int32_t* draft_tokens,
+                                   const int32_t* k_per_req, int32_t* out_accept_len,
+                                   int32_t* out_tokens, void* stream, int32_t batch,
+                                   int64_t target_rows, int32_t vocab, void* workspace,
+                                   size_t workspace_bytes) {
+  if (batch < 0 || target_rows < 0 || vocab < 1 || target_rows >= INT_MAX) return SV_ERR_ARG;
+  if (target_rows < int64_t(batch)) return SV_ERR_ARG;
+  if (!workspace || misaligned(workspace, 256) || workspace_bytes < sizeof(WsHeader))
+    return SV_ERR_WORKSPACE;
+  if (batch == 0) return SV_OK;
+  if (!target_argmax || !k_per_req || !out_accept_len || !out_tokens) return SV_ERR_ARG;
+  if (target_rows > int64_t(batch) && !draft_tokens) return SV_ERR_ARG;
+  return launch_greedy_from_argmax(target_argmax, draft_tokens, k_per_req, out_accept_len,
+                                   out_tokens, batch, target_rows, vocab, workspace,
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? SV_OK
+             : SV_ERR_CUDA;
+}
+
 int spec_verify_get_error(const void* workspace, void* stream, int32_t* code, int32_t* request,
                           int64_t* row) {
   if (!workspace || !code) return SV_ERR_ARG;

@@ -207,6 +207,10 @@ cudaError_t launch_kv_commit(void* cache, const void* spec, int64_t num_pages, i
                              int32_t* kv_len, const int32_t* block_table, int max_pages, int B,
                              void* workspace, int sms, cudaStream_t s);
 cudaError_t launch_sample_post(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_greedy_from_argmax(const int32_t* argmax, const int32_t* draft_tokens,
+                                      const int32_t* k_per_req, int32_t* out_accept_len,
+                                      int32_t* out_tokens, int B, int64_t Rt, int V,
+                                      void* workspace, cudaStream_t s);
 size_t rowpass_smem_bytes();
 
 // Launch of a kernel that may start while the previous kernel on the stream
