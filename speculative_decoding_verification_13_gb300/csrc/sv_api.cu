@@ -158,10 +158,12 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   const int64_t fmax = int64_t(sms) * ds.occ_filter;
   if (launch_filter_decide(P, bf16, int(fjobs < fmax ? fjobs : fmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
-  // draw pass: a queued draw is cut into segments when there are few requests,
-  // so that every SM streams (at most one queued draw per request)
+  // draw pass: a queued draw is cut into segments so that the units (draws x
+  // segments) outnumber the resident CTAs about fourfold and the last round
+  // is short (at most one queued draw per request)
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
-  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, dmax / std::max(batch, 1))));
+  P.n_seg = int(std::max<int64_t>(
+      1, std::min<int64_t>(kMaxSeg, (4 * dmax + batch - 1) / std::max(batch, 1))));
   const int64_t djobs = int64_t(batch) * P.n_seg;
   if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
@@ -241,7 +243,7 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
     return SV_ERR_CUDA;
   // every sampled unfiltered row may queue a draw
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
-  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, dmax / rows)));
+  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, (4 * dmax + rows - 1) / rows)));
   const int64_t djobs = rows * P.n_seg;
   if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
     return SV_ERR_CUDA;

@@ -13,8 +13,9 @@
 // "full" mbarrier; consumer warps release stages on an "empty" mbarrier).
 // The 8 consumer warps turn each 256-element tile into its weight sum (float,
 // a warp scan); once the row is done, one warp adds the tile sums in tile
-// order (double), finds the tile where the prefix first exceeds t = u_k S and
-// scans that tile's elements (re-read from global memory, L2-resident).  The
+// order (exact integers, in units of 2^-40), finds the tile where the prefix
+// first exceeds t = u_k S and scans that tile's elements (re-read from global
+// memory, L2-resident).  The
 // producer runs ahead into the next request while the consumers locate.
 // Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops,
 // and lets the copies it issued land before exiting.
@@ -32,6 +33,8 @@ constexpr int kDConsumerWarps = 8;
 constexpr int kDConsumers = kDConsumerWarps * 32;
 constexpr int kDThreads = kDConsumers + 32;
 constexpr int kDTile = 256;                   // elements per tile (32 lanes x 8)
+// tile sums a row's survivor slot holds past its first 64 bytes
+constexpr int kTileStore = (kRawCap * 8 - 64) / 4;
 constexpr uint32_t kFull = 0xffffffffu;
 
 // Weight of element y.
@@ -42,28 +45,36 @@ constexpr uint32_t kFull = 0xffffffffu;
 // its composite key (logit descending, index ascending) is at least the
 // threshold's: x > v, or x == v and y <= i for the threshold's value v and
 // index i; p or q is 0 outside the kept set.
+// The probabilities are formed as 2^((x - m) c2 - l), x - m exact for bf16
+// logits and one FMA: l = 0 for the unnormalised bonus weights, l = log2 S
+// for normalised p and q (the weights near the row maximum, which carry the
+// mass, keep the accuracy of ex2.approx).
 struct Weights {
   float mt, ist, md, isd, c2;
+  float bt, bd;   // log2 normalisers of the target and draft weights (kind)
+  float bt0, btn; // bonus (unnormalised: 0) and normalised target ones
   int kind;
   bool mask_t, mask_d;
   float vt, vd;
   uint32_t it, id;
+  __device__ __forceinline__ void set_kind(int k) {
+    kind = k;
+    bt = k == 0 ? bt0 : btn;
+  }
   __device__ __forceinline__ float operator()(float xt, float xd) const {
-    const float et = ex2_approx((xt - mt) * c2);
-    if (kind == 0) return et;
-    if (kind == 2) return et * ist;
-    const float ed = ex2_approx((xd - md) * c2);
-    return fmaxf(0.f, et * ist - ed * isd);
+    const float et = ex2_approx(fmaf(xt - mt, c2, -bt));
+    if (kind != 1) return et;
+    const float ed = ex2_approx(fmaf(xd - md, c2, -bd));
+    return fmaxf(0.f, et - ed);
   }
   // the same with the kept-set masks (y: the element's index)
   __device__ __forceinline__ float masked(float xt, float xd, uint32_t y) const {
     const bool kt = !mask_t || xt > vt || (xt == vt && y <= it);
-    const float et = kt ? ex2_approx((xt - mt) * c2) : 0.f;
-    if (kind == 0) return et;
-    if (kind == 2) return et * ist;
+    const float et = kt ? ex2_approx(fmaf(xt - mt, c2, -bt)) : 0.f;
+    if (kind != 1) return et;
     const bool kd = !mask_d || xd > vd || (xd == vd && y <= id);
-    const float ed = kd ? ex2_approx((xd - md) * c2) : 0.f;
-    return fmaxf(0.f, et * ist - ed * isd);
+    const float ed = kd ? ex2_approx(fmaf(xd - md, c2, -bd)) : 0.f;
+    return fmaxf(0.f, et - ed);
   }
   __device__ __forceinline__ float at(float xt, float xd, int y) const {
     return (mask_t || mask_d) ? masked(xt, xd, uint32_t(y)) : (*this)(xt, xd);
@@ -121,8 +132,8 @@ __device__ __forceinline__ void elems8(const unsigned char* fast, const void* ro
 }
 
 struct DrawPassShared {
-  double S;
-  double R;
+  unsigned long long S;  // fixed point (2^-40)
+  unsigned long long R;
   int tstar;
   int fallback;
   int last;
@@ -139,21 +150,33 @@ __device__ __forceinline__ void draw_sync() {
   asm volatile("bar.sync 2, %0;" ::"n"(kDConsumers) : "memory");
 }
 
-__device__ __forceinline__ double warp_scan_d(double v) {
-  const int lane = threadIdx.x & 31;
+// A float weight (or sum of weights) as an integer multiple of 2^-40.
+__device__ __forceinline__ unsigned long long fixw(float x) {
+  return __float2ull_rn(x * 1099511627776.0f);
+}
+
+__device__ __forceinline__ float sum8(const float* r) {
+  return ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+}
+
+// Warp sums (every lane gets the total) and an inclusive warp scan.
+__device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(kFull, v, o);
-    if (lane >= o) v += y;
-  }
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
 }
 
-__device__ __forceinline__ float warp_scan_f(float v) {
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(kFull, v, o);
+    const unsigned long long y = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v += y;
   }
   return v;
@@ -253,28 +276,36 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   }
 
   // ------------------------------------------------------------- consumers
+  // Prefix work is done on fixed-point copies of the float tile sums (units
+  // of 2^-40 of the row's largest weight, as integers): additions in any
+  // order are then exact and cheap, where double additions (the narrow FP64
+  // pipe) set the pace of one warp for microseconds per draw.  A weight is at
+  // most 1 and a tile holds 256, so a tile sum is below 2^48 and a row's
+  // below 2^62.
   const int cwarp = warp - 1;
   uint32_t stage = 0, phase = 0;
-  // tile sum of tile tau read from global memory, with weights W
-  auto tile_from_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau) {
+  // the lane's 8 weights of tile tau, read from global memory (L2)
+  auto lane_tile_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau,
+                              float* r) {
     const int e = tau * kDTile + lane * 8;
     float xt[8], xd[8];
     elems8<BF16>(nullptr, trow, e, 0, V, xt);
     if (Wt.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
-    float ls = 0.f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ls += Wt.at(xt[k], Wt.kind == 1 ? xd[k] : 0.f, e + k);
-    return __shfl_sync(kFull, warp_scan_f(ls), 31);
+    for (int k = 0; k < 8; ++k) r[k] = Wt.at(xt[k], Wt.kind == 1 ? xd[k] : 0.f, e + k);
   };
-  // sum of tiles [a, z) in tile order (double), one warp
-  auto tiles_total = [&](int a, int z) {
-    double tot = 0.0;
-    for (int t0 = a; t0 < z; t0 += 32) {
-      const double v = t0 + lane < z ? double(ts[t0 + lane]) : 0.0;
-      tot = __shfl_sync(kFull, warp_scan_d(v) + tot, 31);
-    }
-    return tot;
+  auto tile_from_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau) {
+    float r[8];
+    lane_tile_global(Wt, trow, drow, tau, r);
+    return warp_sum_f(sum8(r));
   };
+  // sum of tiles [a, z) in fixed point, one warp
+  auto tiles_total = [&](int a, int z) -> unsigned long long {
+    unsigned long long tot = 0ull;
+    for (int t0 = a + lane; t0 < z; t0 += 32) tot += fixw(ts[t0]);
+    return warp_sum_u64(tot);
+  };
+  unsigned long long* seg_fix = reinterpret_cast<unsigned long long*>(w.seg_sum);
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     const int q = u / nseg, sg = u - q * nseg;
     const DrawDesc d = w.draw[q];
@@ -284,7 +315,10 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     W.md = d.md;
     W.isd = d.isd;
     W.c2 = d.c2;
-    W.kind = d.kind;
+    W.bt0 = 0.f;
+    W.btn = -log2f(d.ist);
+    W.bd = d.kind == 1 ? -log2f(d.isd) : 0.f;
+    W.set_kind(d.kind);
     W.mask_t = d.kt != 0ull;
     W.mask_d = d.kind == 1 && d.kd != 0ull;
     W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
@@ -298,7 +332,8 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     int sa, sz, ta, tz;
     seg_stages(sg, &sa, &sz);
     seg_tiles(sg, &ta, &tz);
-    // tile sums of this segment: the tiles of each stage as it lands
+    // tile sums of this segment: the tiles of each stage as it lands, two
+    // tiles per warp at a time (independent sums, reduced side by side)
     for (int s = sa; s < sz; ++s) {
       if (!wait_bar(full0 + 8u * stage, phase, &S.cabort, &S.pabort, 16)) {
         *reinterpret_cast<volatile int*>(&S.cabort) = 1;
@@ -306,25 +341,40 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
       }
       if (!*reinterpret_cast<volatile int*>(&S.cabort)) {
         const unsigned char* tp = ring + size_t(stage) * kDStageBytes;
-        for (int i = cwarp; i < kTPS; i += kDConsumerWarps) {
-          const int tau = s * kTPS + i;
-          if (tau >= ntile) break;
-          const int e = tau * kDTile + lane * 8;
-          const int off = (i * kDTile + lane * 8) * E::kSize;
-          float xt[8], xd[8];
-          elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
-          if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
-          float ls = 0.f;
-          if (W.mask_t || W.mask_d) {
+        for (int i = cwarp; i < kTPS; i += 2 * kDConsumerWarps) {
+          const int i2 = i + kDConsumerWarps;
+          const bool two = i2 < kTPS;
+          float la = 0.f, lb = 0.f;
+          {
+            const int e = (s * kTPS + i) * kDTile + lane * 8;
+            const int off = (i * kDTile + lane * 8) * E::kSize;
+            float xt[8], xd[8], r[8];
+            elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
+            if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              ls += W.masked(xt[k], W.kind == 1 ? xd[k] : 0.f, uint32_t(e + k));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) ls += W(xt[k], W.kind == 1 ? xd[k] : 0.f);
+            for (int k = 0; k < 8; ++k) r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k);
+            la = sum8(r);
           }
-          const float tsum = __shfl_sync(kFull, warp_scan_f(ls), 31);
-          if (lane == 0) ts[tau] = tsum;
+          if (two) {
+            const int e = (s * kTPS + i2) * kDTile + lane * 8;
+            const int off = (i2 * kDTile + lane * 8) * E::kSize;
+            float xt[8], xd[8], r[8];
+            elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
+            if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k);
+            lb = sum8(r);
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            la += __shfl_xor_sync(kFull, la, o);
+            lb += __shfl_xor_sync(kFull, lb, o);
+          }
+          const int tau = s * kTPS + i, tau2 = s * kTPS + i2;
+          if (lane == 0) {
+            if (tau < ntile) ts[tau] = la;
+            if (two && tau2 < ntile) ts[tau2] = lb;
+          }
         }
       }
       __syncwarp();
@@ -341,12 +391,22 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     }
     draw_sync();
     if (*reinterpret_cast<volatile int*>(&S.cabort)) break;
+    // With several segments, each keeps its tile sums in the target row's
+    // survivor slot (unused by rows the draw pass serves, past the 8 bytes of
+    // a kept-set threshold), so that the CTA locating the draw reads the
+    // winning segment's sums there instead of streaming its logits again.
+    const bool gstore = nseg > 1 && ntile <= kTileStore;
+    float* gts = reinterpret_cast<float*>(w.cand_raw + size_t(d.tr) * kRawCap) + 16;
+    if (gstore) {
+      for (int tau = ta + (tid - 32); tau < tz; tau += kDConsumers) gts[tau] = ts[tau];
+      __threadfence();
+    }
     // the segment's sum; the CTA that completes a draw's last segment locates it
     if (cwarp == 0) {
-      const double segsum = tiles_total(ta, tz);
+      const unsigned long long segsum = tiles_total(ta, tz);
       int last = 1;
       if (nseg > 1 && lane == 0) {
-        w.seg_sum[size_t(q) * kMaxSeg + sg] = segsum;
+        seg_fix[size_t(q) * kMaxSeg + sg] = segsum;
         __threadfence();
         last = atomicAdd(&w.seg_cnt[q], 1) == nseg - 1;
       }
@@ -358,50 +418,52 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     draw_sync();
     if (!S.last) continue;
     if (nseg > 1) __threadfence();  // the other segments' sums are read below
-    // total S over the segments, in segment order (one warp)
+    // total S over the segments
     if (cwarp == 0) {
-      double tot = S.S;
-      if (nseg > 1) {
-        const double v = lane < nseg ? __ldcg(&w.seg_sum[size_t(q) * kMaxSeg + lane]) : 0.0;
-        tot = __shfl_sync(kFull, warp_scan_d(v), 31);
-      }
+      unsigned long long tot = S.S;
+      if (nseg > 1)
+        tot = warp_sum_u64(lane < nseg ? __ldcg(&seg_fix[size_t(q) * kMaxSeg + lane]) : 0ull);
       if (lane == 0) {
         S.S = tot;
-        S.fallback = W.kind == 1 && !(tot > 0.0);
+        S.fallback = W.kind == 1 && tot == 0ull;
       }
     }
     draw_sync();
     int nsegL = nseg;  // segments of the sums the search below walks
     if (S.fallback) {
       // residual mass vanished through rounding: draw from p_L, every tile again
-      W.kind = 2;
+      W.set_kind(2);
       for (int tau = cwarp; tau < ntile; tau += kDConsumerWarps) {
         const float tsum = tile_from_global(W, trow, drow, tau);
         if (lane == 0) ts[tau] = tsum;
       }
       draw_sync();
       if (cwarp == 0) {
-        const double tot = tiles_total(0, ntile);
+        const unsigned long long tot = tiles_total(0, ntile);
         if (lane == 0) S.S = tot;
       }
       nsegL = 1;
       draw_sync();
     }
-    const double t = d.u * S.S;
+    // t = floor(u_k S): the draw is the first y whose inclusive prefix
+    // exceeds t (for an integer prefix C, C > u S iff C > floor(u S))
+    const unsigned long long Stot = S.S;
+    const unsigned long long ufix = (unsigned long long)(d.u * 4294967296.0);  // exact
+    const unsigned long long t =
+        (__umul64hi(Stot, ufix) << 32) | ((Stot * ufix) >> 32);
     // the segment whose inclusive prefix first exceeds t (R: the prefix before it)
     if (cwarp == 0) {
       int sstar = 0;
-      double R = 0.0;
+      unsigned long long R = 0ull;
       if (nsegL > 1) {
-        const double v = lane < nseg ? __ldcg(&w.seg_sum[size_t(q) * kMaxSeg + lane]) : 0.0;
-        const double incl = warp_scan_d(v);
-        double ex = __shfl_up_sync(kFull, incl, 1);
-        if (lane == 0) ex = 0.0;
+        const unsigned long long v =
+            lane < nseg ? __ldcg(&seg_fix[size_t(q) * kMaxSeg + lane]) : 0ull;
+        const unsigned long long incl = warp_incl_scan_u64(v);
         const uint32_t hit = __ballot_sync(kFull, lane < nseg && incl > t);
-        const uint32_t pos = __ballot_sync(kFull, lane < nseg && v > 0.0);
+        const uint32_t pos = __ballot_sync(kFull, lane < nseg && v > 0ull);
         const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : nseg - 1);
         sstar = l;
-        R = __shfl_sync(kFull, ex, l);
+        R = __shfl_sync(kFull, incl - v, l);
       }
       if (lane == 0) {
         S.tstar = sstar;
@@ -414,34 +476,38 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     if (nsegL > 1) {
       seg_tiles(sstar, &sa2, &sz2);
       if (sstar != sg) {
-        // that segment's tile sums, recomputed from global memory (L2)
-        for (int tau = sa2 + cwarp; tau < sz2; tau += kDConsumerWarps) {
-          const float tsum = tile_from_global(W, trow, drow, tau);
-          if (lane == 0) ts[tau] = tsum;
+        if (gstore) {
+          // that segment's tile sums, as its CTA stored them
+          for (int tau = sa2 + (tid - 32); tau < sz2; tau += kDConsumers)
+            ts[tau] = __ldcg(gts + tau);
+        } else {
+          // that segment's tile sums, recomputed from global memory
+          for (int tau = sa2 + cwarp; tau < sz2; tau += kDConsumerWarps) {
+            const float tsum = tile_from_global(W, trow, drow, tau);
+            if (lane == 0) ts[tau] = tsum;
+          }
         }
         draw_sync();
       }
     }
     if (cwarp == 0) {
       // the tile where the prefix first exceeds t, then the element in it
-      double carry = S.R, R = S.R, Rlast = S.R;
+      unsigned long long carry = S.R, R = S.R, Rlast = S.R;
       int tstar = -1, tlast = -1;
       for (int t0 = sa2; t0 < sz2 && tstar < 0; t0 += 32) {
-        const double v = t0 + lane < sz2 ? double(ts[t0 + lane]) : 0.0;
-        const double incl = warp_scan_d(v) + carry;
-        double ex = __shfl_up_sync(kFull, incl, 1);
-        if (lane == 0) ex = carry;
-        const uint32_t pos = __ballot_sync(kFull, v > 0.0);
+        const unsigned long long v = t0 + lane < sz2 ? fixw(ts[t0 + lane]) : 0ull;
+        const unsigned long long incl = warp_incl_scan_u64(v) + carry;
+        const uint32_t pos = __ballot_sync(kFull, v > 0ull);
         const uint32_t hit = __ballot_sync(kFull, t0 + lane < sz2 && incl > t);
         if (pos) {
           const int l = 31 - __clz(pos);
           tlast = t0 + l;
-          Rlast = __shfl_sync(kFull, ex, l);
+          Rlast = __shfl_sync(kFull, incl - v, l);
         }
         if (hit) {
           const int l = __ffs(hit) - 1;
           tstar = t0 + l;
-          R = __shfl_sync(kFull, ex, l);
+          R = __shfl_sync(kFull, incl - v, l);
         }
         carry = __shfl_sync(kFull, incl, 31);
       }
@@ -451,26 +517,26 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
       }
       int y = -1;
       if (tstar >= 0) {
+        // the tile's elements in fixed point; the first one whose inclusive
+        // prefix exceeds t, else (the tile's float sum rounded above its
+        // elements' fixed-point sum) the last one with mass
         const int base = tstar * kDTile + lane * 8;
-        float xt[8], xd[8], r[8];
-        elems8<BF16>(nullptr, trow, base, 0, V, xt);
-        if (W.kind == 1) elems8<BF16>(nullptr, drow, base, 0, V, xd);
-        float ls = 0.f;
+        float r[8];
+        lane_tile_global(W, trow, drow, tstar, r);
+        unsigned long long wf[8], ls = 0ull;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, base + k);
-          ls += r[k];
+          wf[k] = fixw(r[k]);
+          ls += wf[k];
         }
-        const float inc = warp_scan_f(ls);
-        float exf = __shfl_up_sync(kFull, inc, 1);
-        if (lane == 0) exf = 0.f;
+        const unsigned long long ex = warp_incl_scan_u64(ls) - ls;
         int ye = INT_MAX, lastp = -1;
-        float pre = 0.f;
+        unsigned long long pre = R + ex;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          pre += r[k];
+          pre += wf[k];
           if (r[k] > 0.f) lastp = base + k;
-          if (ye == INT_MAX && r[k] > 0.f && R + double(exf + pre) > t) ye = base + k;
+          if (ye == INT_MAX && wf[k] > 0ull && pre > t) ye = base + k;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
