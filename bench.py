@@ -70,7 +70,7 @@ def workload_desc(config, variant, batch=None):
     return config
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "rowpass_c4_traffic.json")
-KERNEL_SOURCES = ["sv_internal.cuh", "sv_select.cuh", "sv_rowpass.cu"]
+KERNEL_SOURCES = ["sv_internal.cuh", "sv_select.cuh", "sv_bigrow.cuh", "sv_rowpass.cu"]
 
 
 def parse():
