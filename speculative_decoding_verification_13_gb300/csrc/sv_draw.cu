@@ -6,17 +6,21 @@
 //   p_k after a full acceptance (the bonus token),
 // with p and q zero outside their rows' kept sets.
 //
-// Persistent CTAs, one queued request at a time per CTA.  As in the row pass,
-// warp 0 is a producer that streams the request's target row (and draft row,
-// for a residual) through a 4-stage shared-memory ring with TMA bulk copies
-// (cp.async.bulk, one 8 KB piece of each row per stage, completing on a
-// "full" mbarrier; consumer warps release stages on an "empty" mbarrier).
-// The 8 consumer warps turn each 256-element tile into its weight sum (float,
-// a warp scan); once the row is done, one warp adds the tile sums in tile
-// order (exact integers, in units of 2^-40), finds the tile where the prefix
-// first exceeds t = u_k S and scans that tile's elements (re-read from global
-// memory, L2-resident).  The
-// producer runs ahead into the next request while the consumers locate.
+// Persistent CTAs.  A queued draw is cut into segments of whole stages; a
+// unit of work is one segment, and CTAs claim units from a counter.  As in
+// the row pass, warp 0 is a producer that streams the unit's piece of the
+// target row (and of the draft row, for a residual) through a 4-stage
+// shared-memory ring with TMA bulk copies (cp.async.bulk, one 8 KB piece of
+// each row per stage, completing on a "full" mbarrier; consumer warps release
+// stages on an "empty" mbarrier), with the unit and its descriptor in a slot
+// per stage.  The 8 consumer warps turn each 256-element tile into its weight
+// sum (float; packed f32x2 arithmetic for rows without a kept-set mask); the
+// segment's sum goes to global memory, and the CTA that finishes a draw's
+// last segment adds the segment sums and the crossing segment's tile sums
+// (exact integers, in units of 2^-40), finds the tile where the prefix first
+// exceeds t = u_k S and scans that tile's elements (re-read from global
+// memory, L2-resident).  The producer runs ahead into the next unit while the
+// consumers locate.
 // Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops,
 // and lets the copies it issued land before exiting.
 #include <math.h>
@@ -182,6 +186,123 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return v;
 }
 
+// Packed pairs of floats for the f32x2 instructions (two IEEE round-to-nearest
+// operations each, bit for bit those of the scalar forms), so that the weight
+// of two elements costs one subtraction and one FMA issue instead of two each.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// bf16 elements 2j, 2j+1 of 16 bytes (one 32-bit word) as a packed pair.
+__device__ __forceinline__ uint64_t bf16_pair(const uint4& q, int j) {
+  const uint32_t w = j == 0 ? q.x : j == 1 ? q.y : j == 2 ? q.z : q.w;
+  return pk2(bf16_lo(w), bf16_hi(w));
+}
+
+// Weight sum of a lane's 8 consecutive elements of an unmasked row pair, the
+// loop-invariant parts (m, c2, log2 normaliser) packed once per draw:
+//   KIND 0: 2^((x_t - m_t) c2 - b_t)
+//   KIND 1: max(0, 2^((x_t - m_t) c2 - b_t) - 2^((x_d - m_d) c2 - b_d))
+// The same per-element weights as Weights::operator(); the 8 are summed as
+// pairs, then the pair's halves.
+struct PackedW {
+  uint64_t mt, md, c2, nbt, nbd;
+};
+
+template <int KIND>
+__device__ __forceinline__ float lane8_sum_bf16(const PackedW& pw, const unsigned char* tp,
+                                                const unsigned char* dp) {
+  const uint4 qt = *reinterpret_cast<const uint4*>(tp);
+  uint4 qd = make_uint4(0u, 0u, 0u, 0u);
+  if (KIND == 1) qd = *reinterpret_cast<const uint4*>(dp);
+  uint64_t r[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float a0, a1;
+    upk2(fma2(sub2(bf16_pair(qt, j), pw.mt), pw.c2, pw.nbt), a0, a1);
+    float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+    if (KIND == 1) {
+      float b0, b1;
+      upk2(fma2(sub2(bf16_pair(qd, j), pw.md), pw.c2, pw.nbd), b0, b1);
+      float d0, d1;
+      upk2(sub2(pk2(e0, e1), pk2(ex2_approx(b0), ex2_approx(b1))), d0, d1);
+      e0 = fmaxf(0.f, d0);
+      e1 = fmaxf(0.f, d1);
+    }
+    r[j] = pk2(e0, e1);
+  }
+  float lo, hi;
+  upk2(add2(add2(r[0], r[1]), add2(r[2], r[3])), lo, hi);
+  return lo + hi;
+}
+
+template <int KIND>
+__device__ __forceinline__ float lane8_sum_f32(const PackedW& pw, const unsigned char* tp,
+                                               const unsigned char* dp) {
+  const uint4* t4 = reinterpret_cast<const uint4*>(tp);
+  const uint4* d4 = reinterpret_cast<const uint4*>(dp);
+  uint64_t r[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint4 qt = t4[h];
+    uint4 qd = make_uint4(0u, 0u, 0u, 0u);
+    if (KIND == 1) qd = d4[h];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint64_t xt = j == 0 ? (uint64_t(qt.y) << 32 | qt.x) : (uint64_t(qt.w) << 32 | qt.z);
+      float a0, a1;
+      upk2(fma2(sub2(xt, pw.mt), pw.c2, pw.nbt), a0, a1);
+      float e0 = ex2_approx(a0), e1 = ex2_approx(a1);
+      if (KIND == 1) {
+        const uint64_t xd =
+            j == 0 ? (uint64_t(qd.y) << 32 | qd.x) : (uint64_t(qd.w) << 32 | qd.z);
+        float b0, b1;
+        upk2(fma2(sub2(xd, pw.md), pw.c2, pw.nbd), b0, b1);
+        float d0, d1;
+        upk2(sub2(pk2(e0, e1), pk2(ex2_approx(b0), ex2_approx(b1))), d0, d1);
+        e0 = fmaxf(0.f, d0);
+        e1 = fmaxf(0.f, d1);
+      }
+      r[2 * h + j] = pk2(e0, e1);
+    }
+  }
+  float lo, hi;
+  upk2(add2(add2(r[0], r[1]), add2(r[2], r[3])), lo, hi);
+  return lo + hi;
+}
+
+template <bool BF16, int KIND>
+__device__ __forceinline__ float lane8_sum(const PackedW& pw, const unsigned char* tp,
+                                           const unsigned char* dp) {
+  return BF16 ? lane8_sum_bf16<KIND>(pw, tp, dp) : lane8_sum_f32<KIND>(pw, tp, dp);
+}
+
+// Stage slot: what the producer armed a ring phase with.
+struct StageSlot {
+  int32_t unit;  // queued draw x segments index, or -1: no more work
+  int32_t s;     // the stage of the row the phase carries, or -1: a phase with no copy
+};
+
 template <bool BF16>
 __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P) {
   using E = Elt<BF16>;
@@ -189,6 +310,8 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   constexpr int kTPS = kEPS / kDTile;      // tiles per stage
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ DrawPassShared S;
+  __shared__ StageSlot slot[kDStages];
+  __shared__ DrawDesc sdesc[kDStages];
   unsigned char* ring = smem;
   const uint32_t full0 = smem_addr(smem + size_t(kDStages) * kDStageBytes);
   const uint32_t empty0 = full0 + 8u * kDStages;
@@ -212,10 +335,14 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   const int64_t bulk = (int64_t(V) * E::kSize) & ~int64_t(15);
   const int nst = int((bulk + kDHalf - 1) / kDHalf);
   const int fast_end = int(bulk / E::kSize);  // elements the bulk copies deliver
-  // Each queued draw is cut into nseg segments of whole stages (the last one
-  // also owns the tiles past the bulk-copied part); a unit is one segment.
-  const int nseg = max(1, min(P.n_seg, nst));
-  const int sps = nst > 0 ? (nst + nseg - 1) / nseg : 0;  // stages per segment
+  // Each queued draw is cut into nseg segments of sps whole stages (the last
+  // one also owns the tiles past the bulk-copied part; none is empty); a unit
+  // is one segment.  CTA i starts with unit i and claims further units from a
+  // counter, so that CTAs whose units were bonus draws (one row) or finished
+  // early take more.
+  const int nseg0 = max(1, min(P.n_seg, nst));
+  const int sps = nst > 0 ? (nst + nseg0 - 1) / nseg0 : 0;  // stages per segment
+  const int nseg = sps > 0 ? (nst + sps - 1) / sps : 1;
   const int units = n_draw * nseg;
   auto seg_stages = [&](int s, int* a, int* z) {
     *a = min(nst, s * sps);
@@ -227,42 +354,65 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   };
 
   // ------------------------------------------------------------- producer
+  // Arms one ring phase per stage of each unit it claims (a phase with no copy
+  // for a unit without bulk stages), after writing the phase's slot: the unit,
+  // the stage and the draw's descriptor, which the consumers read once the
+  // phase completes (the arrival releases the writes).  A last phase with unit
+  // -1 tells the consumers that the work is done.
   if (warp == 0) {
     if (lane != 0) return;
     uint32_t stage = 0, phase = 0;
     long long issued = 0;
     bool stop = false;
-    for (int u = blockIdx.x; u < units && !stop; u += gridDim.x) {
-      const int q = u / nseg, sg = u - q * nseg;
-      const DrawDesc d = w.draw[q];
-      const char* tsrc = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
-      const char* dsrc = d.kind == 1 ? static_cast<const char*>(P.draft) +
-                                           (d.dr - P.Rt) * P.d_stride * E::kSize
-                                     : nullptr;
-      int sa, sz;
-      seg_stages(sg, &sa, &sz);
-      for (int s = sa; s < sz; ++s) {
-        const int64_t rem = bulk - int64_t(s) * kDHalf;
-        const uint32_t bytes = uint32_t(rem < kDHalf ? rem : kDHalf);
+    const uint64_t pol = l2_evict_first_policy();
+    int u = blockIdx.x;
+    while (!stop) {
+      const bool live = u < units;
+      // the next unit, claimed now: the atomic's round trip overlaps this unit's copies
+      const int next = live ? int(gridDim.x) + atomicAdd(&w.hdr->dp_next, 1) : units;
+      DrawDesc d{};
+      int sa = 0, sz = 0;
+      const char* tsrc = nullptr;
+      const char* dsrc = nullptr;
+      if (live) {
+        const int q = u / nseg, sg = u - q * nseg;
+        d = w.draw[q];
+        seg_stages(sg, &sa, &sz);
+        tsrc = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
+        if (d.kind == 1)
+          dsrc = static_cast<const char*>(P.draft) + (d.dr - P.Rt) * P.d_stride * E::kSize;
+      }
+      int s = sa;
+      do {
         if (!wait_bar(empty0 + 8u * stage, phase ^ 1u, &S.cabort, &S.pabort, 64)) {
           *reinterpret_cast<volatile int*>(&S.pabort) = 1;
-          record_error(w.hdr, SV_ERR_TIMEOUT, -1, d.tr);
+          record_error(w.hdr, SV_ERR_TIMEOUT, -1, live ? d.tr : -1);
           stop = true;
           break;
         }
         const uint32_t full = full0 + 8u * stage;
-        mbar_arrive_expect_tx(full, dsrc ? 2u * bytes : bytes);
-        unsigned char* dst = ring + size_t(stage) * kDStageBytes;
-        const uint64_t pol = l2_evict_first_policy();
-        bulk_load_hint(smem_addr(dst), tsrc + int64_t(s) * kDHalf, bytes, full, pol);
-        if (dsrc)
-          bulk_load_hint(smem_addr(dst + kDHalf), dsrc + int64_t(s) * kDHalf, bytes, full, pol);
+        const bool copy = live && s < sz;
+        slot[stage] = StageSlot{live ? u : -1, copy ? s : -1};
+        if (live) sdesc[stage] = d;
+        if (copy) {
+          const int64_t rem = bulk - int64_t(s) * kDHalf;
+          const uint32_t bytes = uint32_t(rem < kDHalf ? rem : kDHalf);
+          mbar_arrive_expect_tx(full, dsrc ? 2u * bytes : bytes);
+          unsigned char* dst = ring + size_t(stage) * kDStageBytes;
+          bulk_load_hint(smem_addr(dst), tsrc + int64_t(s) * kDHalf, bytes, full, pol);
+          if (dsrc)
+            bulk_load_hint(smem_addr(dst + kDHalf), dsrc + int64_t(s) * kDHalf, bytes, full, pol);
+        } else {
+          mbar_arrive(full);
+        }
         ++issued;
         if (++stage == kDStages) {
           stage = 0;
           phase ^= 1u;
         }
-      }
+      } while (++s < sz);
+      if (!live) break;
+      u = next;
     }
     if (stop || *reinterpret_cast<volatile int*>(&S.cabort)) {
       // Let every copy this CTA issued land before the CTA may exit.
@@ -306,65 +456,86 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     return warp_sum_u64(tot);
   };
   unsigned long long* seg_fix = reinterpret_cast<unsigned long long*>(w.seg_sum);
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const int q = u / nseg, sg = u - q * nseg;
-    const DrawDesc d = w.draw[q];
-    Weights W;
-    W.mt = d.mt;
-    W.ist = d.ist;
-    W.md = d.md;
-    W.isd = d.isd;
-    W.c2 = d.c2;
-    W.bt0 = 0.f;
-    W.btn = -log2f(d.ist);
-    W.bd = d.kind == 1 ? -log2f(d.isd) : 0.f;
-    W.set_kind(d.kind);
-    W.mask_t = d.kt != 0ull;
-    W.mask_d = d.kind == 1 && d.kd != 0ull;
-    W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
-    W.vd = W.mask_d ? composite_value(d.kd) : 0.f;
-    W.it = uint32_t(composite_index(d.kt));
-    W.id = uint32_t(composite_index(d.kd));
-    const void* trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
-    const void* drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
-                                         (d.dr - P.Rt) * P.d_stride * E::kSize
-                                   : nullptr;
-    int sa, sz, ta, tz;
-    seg_stages(sg, &sa, &sz);
-    seg_tiles(sg, &ta, &tz);
-    // tile sums of this segment: the tiles of each stage as it lands, two
-    // tiles per warp at a time (independent sums, reduced side by side)
-    for (int s = sa; s < sz; ++s) {
+  int cur = -1;  // the unit being summed
+  Weights W{};
+  bool fast = true;  // no kept-set mask: the packed path
+  int q = 0, sg = 0, sa = 0, sz = 0, ta = 0, tz = 0;
+  const void* trow = nullptr;
+  const void* drow = nullptr;
+  for (;;) {
+    // The phases of one unit.  Every consumer warp leaves this loop for the
+    // barrier below exactly once per unit: after the unit's last phase, at the
+    // end marker, or after a wait that gave up (which makes every later wait
+    // give up at once), so that the named barriers below always match.
+    bool end = false;
+    for (;;) {
       if (!wait_bar(full0 + 8u * stage, phase, &S.cabort, &S.pabort, 16)) {
         *reinterpret_cast<volatile int*>(&S.cabort) = 1;
-        record_error(w.hdr, SV_ERR_TIMEOUT, -1, d.tr);
+        record_error(w.hdr, SV_ERR_TIMEOUT, -1, -1);
+        break;
       }
-      if (!*reinterpret_cast<volatile int*>(&S.cabort)) {
+      const StageSlot sl = slot[stage];
+      if (sl.unit < 0) {
+        end = true;
+        break;
+      }
+      if (sl.unit != cur) {
+        cur = sl.unit;
+        const DrawDesc d = sdesc[stage];
+        q = cur / nseg;
+        sg = cur - q * nseg;
+        W.mt = d.mt;
+        W.ist = d.ist;
+        W.md = d.md;
+        W.isd = d.isd;
+        W.c2 = d.c2;
+        W.bt0 = 0.f;
+        W.btn = -log2f(d.ist);
+        W.bd = d.kind == 1 ? -log2f(d.isd) : 0.f;
+        W.set_kind(d.kind);
+        W.mask_t = d.kt != 0ull;
+        W.mask_d = d.kind == 1 && d.kd != 0ull;
+        W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
+        W.vd = W.mask_d ? composite_value(d.kd) : 0.f;
+        W.it = uint32_t(composite_index(d.kt));
+        W.id = uint32_t(composite_index(d.kd));
+        fast = !W.mask_t && !W.mask_d;
+        trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
+        drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
+                                 (d.dr - P.Rt) * P.d_stride * E::kSize
+                           : nullptr;
+        seg_stages(sg, &sa, &sz);
+        seg_tiles(sg, &ta, &tz);
+      }
+      if (sl.s >= 0) {
+        // the stage's tiles, two per warp at a time (independent sums,
+        // reduced side by side)
+        const int s = sl.s;
         const unsigned char* tp = ring + size_t(stage) * kDStageBytes;
+        PackedW pw;
+        pw.mt = pk2(W.mt, W.mt);
+        pw.md = pk2(W.md, W.md);
+        pw.c2 = pk2(W.c2, W.c2);
+        pw.nbt = pk2(-W.bt, -W.bt);
+        pw.nbd = pk2(-W.bd, -W.bd);
+        auto lane_sum = [&](int i) -> float {
+          const int e = (s * kTPS + i) * kDTile + lane * 8;
+          const int off = (i * kDTile + lane * 8) * E::kSize;
+          if (fast && e + 8 <= fast_end)
+            return W.kind == 1 ? lane8_sum<BF16, 1>(pw, tp + off, tp + kDHalf + off)
+                               : lane8_sum<BF16, 0>(pw, tp + off, tp + off);
+          float xt[8], xd[8], r[8];
+          elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
+          if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k);
+          return sum8(r);
+        };
         for (int i = cwarp; i < kTPS; i += 2 * kDConsumerWarps) {
           const int i2 = i + kDConsumerWarps;
           const bool two = i2 < kTPS;
-          float la = 0.f, lb = 0.f;
-          {
-            const int e = (s * kTPS + i) * kDTile + lane * 8;
-            const int off = (i * kDTile + lane * 8) * E::kSize;
-            float xt[8], xd[8], r[8];
-            elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
-            if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k);
-            la = sum8(r);
-          }
-          if (two) {
-            const int e = (s * kTPS + i2) * kDTile + lane * 8;
-            const int off = (i2 * kDTile + lane * 8) * E::kSize;
-            float xt[8], xd[8], r[8];
-            elems8<BF16>(tp + off, trow, e, fast_end, V, xt);
-            if (W.kind == 1) elems8<BF16>(tp + kDHalf + off, drow, e, fast_end, V, xd);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) r[k] = W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k);
-            lb = sum8(r);
-          }
+          float la = lane_sum(i);
+          float lb = two ? lane_sum(i2) : 0.f;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             la += __shfl_xor_sync(kFull, la, o);
@@ -383,14 +554,18 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
         stage = 0;
         phase ^= 1u;
       }
+      if (sl.s < 0 || sl.s == sz - 1) break;
     }
+    const bool run = !end && !*reinterpret_cast<volatile int*>(&S.cabort);
     // tiles past the bulk-copied part of the row (last segment), from global memory
-    for (int tau = max(ta, nst * kTPS) + cwarp; tau < tz; tau += kDConsumerWarps) {
-      const float tsum = tile_from_global(W, trow, drow, tau);
-      if (lane == 0) ts[tau] = tsum;
-    }
+    if (run)
+      for (int tau = max(ta, nst * kTPS) + cwarp; tau < tz; tau += kDConsumerWarps) {
+        const float tsum = tile_from_global(W, trow, drow, tau);
+        if (lane == 0) ts[tau] = tsum;
+      }
     draw_sync();
-    if (*reinterpret_cast<volatile int*>(&S.cabort)) break;
+    if (end || *reinterpret_cast<volatile int*>(&S.cabort)) break;
+    const DrawDesc d = w.draw[q];
     // With several segments, each keeps its tile sums in the target row's
     // survivor slot (unused by rows the draw pass serves, past the 8 bytes of
     // a kept-set threshold), so that the CTA locating the draw reads the

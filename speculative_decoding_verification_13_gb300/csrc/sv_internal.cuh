@@ -53,7 +53,8 @@ struct WsHeader {
   int32_t rp_next;      // row pass: rows claimed past each CTA's first
   int32_t n_big;        // kBig rows, listed from the end of the row list
   int32_t rp_next_big;  // row pass over the kBig rows: rows claimed past each CTA's first
-  int32_t pad[3];
+  int32_t dp_next;      // draw pass: units claimed past each CTA's first
+  int32_t pad[2];
 };
 
 struct RowStat {

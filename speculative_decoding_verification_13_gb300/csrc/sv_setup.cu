@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
       w.hdr->rp_next = 0;
       w.hdr->n_big = 0;
       w.hdr->rp_next_big = 0;
+      w.hdr->dp_next = 0;
     }
     s_bad = 0;
   }
@@ -300,6 +301,7 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
     w.hdr->rp_next = 0;
     w.hdr->n_big = 0;
     w.hdr->rp_next_big = 0;
+    w.hdr->dp_next = 0;
   }
   if (threadIdx.x == 0) s_bad = 0;
   // every row may queue a draw: their segment counters start at zero
