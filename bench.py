@@ -455,7 +455,7 @@ def run_sampler(args, ws, rank, local):
                      "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
                      "launch_ms": rowpass_ms, "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 6 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -888,7 +888,7 @@ def main():
                      "bytes_per_launch": bytes_req, "launch_ms": rowpass_ms,
                      "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 6 * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "parity": parity,

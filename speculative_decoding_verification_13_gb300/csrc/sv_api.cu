@@ -17,7 +17,7 @@ namespace sv {
 cudaError_t rowpass_configure();
 cudaError_t filter_occupancy(int* occ);
 cudaError_t draw_configure();
-cudaError_t draw_occupancy(int V, int* occ);
+cudaError_t draw_occupancy(int V, int* occ, int* occ_locate);
 }  // namespace sv
 
 using namespace sv;
@@ -30,6 +30,7 @@ struct DeviceState {
   int sms = 0;
   int occ_filter = 1;  // resident filter / decide CTAs per SM
   int occ_draw = 1;    // resident draw CTAs per SM for vocabulary draw_v
+  int occ_locate = 1;  // resident locate CTAs per SM for vocabulary draw_v
   int draw_v = -1;
   bool ready = false;
 };
@@ -56,9 +57,10 @@ int prepare_device(int vocab, DeviceState* out) {
     g_dev[dev].ready = true;
   }
   if (g_dev[dev].draw_v != vocab) {
-    int od = 1;
-    if (draw_occupancy(vocab, &od) != cudaSuccess) return SV_ERR_CUDA;
+    int od = 1, ol = 1;
+    if (draw_occupancy(vocab, &od, &ol) != cudaSuccess) return SV_ERR_CUDA;
     g_dev[dev].occ_draw = od;
+    g_dev[dev].occ_locate = ol;
     g_dev[dev].draw_v = vocab;
   }
   *out = g_dev[dev];
@@ -159,13 +161,16 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   if (launch_filter_decide(P, bf16, int(fjobs < fmax ? fjobs : fmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
   // draw pass: a queued draw is cut into segments so that the units (draws x
-  // segments) outnumber the resident CTAs about fourfold and the last round
-  // is short (at most one queued draw per request)
+  // segments) outnumber the resident CTAs about kDrawUnitsPerCta-fold and the
+  // last round is short (at most one queued draw per request); then the
+  // locate kernel, one CTA per queued draw
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
   P.n_seg = int(std::max<int64_t>(
-      1, std::min<int64_t>(kMaxSeg, (4 * dmax + batch - 1) / std::max(batch, 1))));
+      1, std::min<int64_t>(kMaxSeg, (kDrawUnitsPerCta * dmax + batch - 1) / std::max(batch, 1))));
   const int64_t djobs = int64_t(batch) * P.n_seg;
-  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
+  const int64_t lmax = int64_t(sms) * ds.occ_locate;
+  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess ||
+      launch_locate(P, bf16, int(batch < lmax ? batch : lmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }
@@ -243,9 +248,12 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
     return SV_ERR_CUDA;
   // every sampled unfiltered row may queue a draw
   const int64_t dmax = int64_t(sms) * ds.occ_draw;
-  P.n_seg = int(std::max<int64_t>(1, std::min<int64_t>(kMaxSeg, (4 * dmax + rows - 1) / rows)));
+  P.n_seg = int(std::max<int64_t>(
+      1, std::min<int64_t>(kMaxSeg, (kDrawUnitsPerCta * dmax + rows - 1) / rows)));
   const int64_t djobs = rows * P.n_seg;
-  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess)
+  const int64_t lmax = int64_t(sms) * ds.occ_locate;
+  if (launch_draw(P, bf16, int(djobs < dmax ? djobs : dmax), s) != cudaSuccess ||
+      launch_locate(P, bf16, int(rows < lmax ? rows : lmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }

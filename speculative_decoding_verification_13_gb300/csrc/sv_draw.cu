@@ -6,21 +6,21 @@
 //   p_k after a full acceptance (the bonus token),
 // with p and q zero outside their rows' kept sets.
 //
-// Persistent CTAs.  A queued draw is cut into segments of whole stages; a
-// unit of work is one segment, and CTAs claim units from a counter.  As in
-// the row pass, warp 0 is a producer that streams the unit's piece of the
-// target row (and of the draft row, for a residual) through a 4-stage
-// shared-memory ring with TMA bulk copies (cp.async.bulk, one 8 KB piece of
-// each row per stage, completing on a "full" mbarrier; consumer warps release
-// stages on an "empty" mbarrier), with the unit and its descriptor in a slot
-// per stage.  The 8 consumer warps turn each 256-element tile into its weight
-// sum (float; packed f32x2 arithmetic for rows without a kept-set mask); the
-// segment's sum goes to global memory, and the CTA that finishes a draw's
-// last segment adds the segment sums and the crossing segment's tile sums
-// (exact integers, in units of 2^-40), finds the tile where the prefix first
-// exceeds t = u_k S and scans that tile's elements (re-read from global
-// memory, L2-resident).  The producer runs ahead into the next unit while the
-// consumers locate.
+// Two kernels.  The draw pass (persistent CTAs) cuts each queued draw into
+// segments of whole stages; a unit of work is one segment, and CTAs claim
+// units from a counter.  As in the row pass, warp 0 is a producer that
+// streams the unit's piece of the target row (and of the draft row, for a
+// residual) through a 4-stage shared-memory ring with TMA bulk copies
+// (cp.async.bulk, one 8 KB piece of each row per stage, completing on a
+// "full" mbarrier; consumer warps release stages on an "empty" mbarrier),
+// with the unit and its descriptor in a slot per stage.  The 8 consumer warps
+// turn each 256-element tile into its weight sum (float; packed f32x2
+// arithmetic for rows without a kept-set mask) and store the segment's tile
+// sums and its total (an exact integer in units of 2^-40) to global memory.
+// The locate kernel then takes each draw from those sums alone: the segment,
+// the tile and the element where the prefix first exceeds t = u_k S, with
+// only the crossing tile's elements read again.  Nothing in the draw pass
+// waits for another CTA.
 // Every wait is bounded; on expiry the kernel records SV_ERR_TIMEOUT, stops,
 // and lets the copies it issued land before exiting.
 #include <math.h>
@@ -136,13 +136,8 @@ __device__ __forceinline__ void elems8(const unsigned char* fast, const void* ro
 }
 
 struct DrawPassShared {
-  unsigned long long S;  // fixed point (2^-40)
-  unsigned long long R;
-  int tstar;
-  int fallback;
-  int last;
-  int cabort;
-  int pabort;
+  int cabort;  // a consumer wait gave up
+  int pabort;  // the producer's wait gave up
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const int* f1,
@@ -297,6 +292,80 @@ __device__ __forceinline__ float lane8_sum(const PackedW& pw, const unsigned cha
   return BF16 ? lane8_sum_bf16<KIND>(pw, tp, dp) : lane8_sum_f32<KIND>(pw, tp, dp);
 }
 
+// The weights of a queued draw, from its descriptor.
+__device__ __forceinline__ Weights make_weights(const DrawDesc& d) {
+  Weights W;
+  W.mt = d.mt;
+  W.ist = d.ist;
+  W.md = d.md;
+  W.isd = d.isd;
+  W.c2 = d.c2;
+  W.bt0 = 0.f;
+  W.btn = -log2f(d.ist);
+  W.bd = d.kind == 1 ? -log2f(d.isd) : 0.f;
+  W.set_kind(d.kind);
+  W.mask_t = d.kt != 0ull;
+  W.mask_d = d.kind == 1 && d.kd != 0ull;
+  W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
+  W.vd = W.mask_d ? composite_value(d.kd) : 0.f;
+  W.it = uint32_t(composite_index(d.kt));
+  W.id = uint32_t(composite_index(d.kd));
+  return W;
+}
+
+// The lane's 8 weights of tile tau, read from global memory.
+template <bool BF16>
+__device__ __forceinline__ void lane_tile_global(const Weights& Wt, const void* trow,
+                                                 const void* drow, int tau, int V, float* r) {
+  const int e = tau * kDTile + (threadIdx.x & 31) * 8;
+  float xt[8], xd[8];
+  elems8<BF16>(nullptr, trow, e, 0, V, xt);
+  if (Wt.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) r[k] = Wt.at(xt[k], Wt.kind == 1 ? xd[k] : 0.f, e + k);
+}
+
+// A tile's weight sum from global memory (one warp; every lane gets it).
+template <bool BF16>
+__device__ __forceinline__ float tile_from_global(const Weights& Wt, const void* trow,
+                                                  const void* drow, int tau, int V) {
+  float r[8];
+  lane_tile_global<BF16>(Wt, trow, drow, tau, V, r);
+  return warp_sum_f(sum8(r));
+}
+
+// How a row of V elements is cut into stages, tiles and segments (the draw
+// pass and the locate kernel must agree): nst bulk-copied stages of
+// kDHalf bytes (fast_end elements), ntile tiles of kDTile, nseg segments of
+// sps whole stages each, none empty (the last one also owns the tiles past
+// the bulk-copied part).
+struct DrawSegs {
+  int nst, ntile, fast_end, sps, nseg, tps;
+  int64_t bulk;
+  __device__ void stages(int s, int* a, int* z) const {
+    *a = min(nst, s * sps);
+    *z = min(nst, (s + 1) * sps);
+  }
+  __device__ void tiles(int s, int* a, int* z) const {
+    *a = min(ntile, s * sps * tps);
+    *z = s == nseg - 1 ? ntile : min(ntile, (s + 1) * sps * tps);
+  }
+};
+
+template <int kSize>
+__device__ __forceinline__ DrawSegs draw_segs(int V, int n_seg) {
+  DrawSegs g;
+  g.ntile = (V + kDTile - 1) / kDTile;
+  g.bulk = (int64_t(V) * kSize) & ~int64_t(15);
+  g.nst = int((g.bulk + kDHalf - 1) / kDHalf);
+  g.fast_end = int(g.bulk / kSize);
+  const int nseg0 = max(1, min(n_seg, g.nst));
+  g.sps = g.nst > 0 ? (g.nst + nseg0 - 1) / nseg0 : 0;
+  g.nseg = g.sps > 0 ? (g.nst + g.sps - 1) / g.sps : 1;
+  g.tps = kDHalf / kSize / kDTile;
+  return g;
+}
+
 // Stage slot: what the producer armed a ring phase with.
 struct StageSlot {
   int32_t unit;  // queued draw x segments index, or -1: no more work
@@ -312,6 +381,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   __shared__ DrawPassShared S;
   __shared__ StageSlot slot[kDStages];
   __shared__ DrawDesc sdesc[kDStages];
+  __shared__ DrawDesc cdesc;  // the consumers' current unit
   unsigned char* ring = smem;
   const uint32_t full0 = smem_addr(smem + size_t(kDStages) * kDStageBytes);
   const uint32_t empty0 = full0 + 8u * kDStages;
@@ -328,30 +398,20 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     S.pabort = 0;
   }
   __syncthreads();
-  pdl_wait();  // the filter / decide kernel's queue
+  pdl_trigger();  // the locate kernel may launch; it waits for this one
+  pdl_wait();     // the filter / decide kernel's queue
   const int n_draw = w.hdr->n_draw;
   const int V = P.V;
-  const int ntile = (V + kDTile - 1) / kDTile;
-  const int64_t bulk = (int64_t(V) * E::kSize) & ~int64_t(15);
-  const int nst = int((bulk + kDHalf - 1) / kDHalf);
-  const int fast_end = int(bulk / E::kSize);  // elements the bulk copies deliver
-  // Each queued draw is cut into nseg segments of sps whole stages (the last
-  // one also owns the tiles past the bulk-copied part; none is empty); a unit
-  // is one segment.  CTA i starts with unit i and claims further units from a
+  // Each queued draw is cut into nseg segments of whole stages; a unit is one
+  // segment.  CTA i starts with unit i and claims further units from a
   // counter, so that CTAs whose units were bonus draws (one row) or finished
   // early take more.
-  const int nseg0 = max(1, min(P.n_seg, nst));
-  const int sps = nst > 0 ? (nst + nseg0 - 1) / nseg0 : 0;  // stages per segment
-  const int nseg = sps > 0 ? (nst + sps - 1) / sps : 1;
+  const DrawSegs g = draw_segs<E::kSize>(V, P.n_seg);
+  const int ntile = g.ntile, nst = g.nst, nseg = g.nseg, fast_end = g.fast_end;
+  const int64_t bulk = g.bulk;
   const int units = n_draw * nseg;
-  auto seg_stages = [&](int s, int* a, int* z) {
-    *a = min(nst, s * sps);
-    *z = min(nst, (s + 1) * sps);
-  };
-  auto seg_tiles = [&](int s, int* a, int* z) {
-    *a = min(ntile, s * sps * kTPS);
-    *z = s == nseg - 1 ? ntile : min(ntile, (s + 1) * sps * kTPS);
-  };
+  auto seg_stages = [&](int s, int* a, int* z) { g.stages(s, a, z); };
+  auto seg_tiles = [&](int s, int* a, int* z) { g.tiles(s, a, z); };
 
   // ------------------------------------------------------------- producer
   // Arms one ring phase per stage of each unit it claims (a phase with no copy
@@ -434,21 +494,6 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
   // below 2^62.
   const int cwarp = warp - 1;
   uint32_t stage = 0, phase = 0;
-  // the lane's 8 weights of tile tau, read from global memory (L2)
-  auto lane_tile_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau,
-                              float* r) {
-    const int e = tau * kDTile + lane * 8;
-    float xt[8], xd[8];
-    elems8<BF16>(nullptr, trow, e, 0, V, xt);
-    if (Wt.kind == 1) elems8<BF16>(nullptr, drow, e, 0, V, xd);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = Wt.at(xt[k], Wt.kind == 1 ? xd[k] : 0.f, e + k);
-  };
-  auto tile_from_global = [&](const Weights& Wt, const void* trow, const void* drow, int tau) {
-    float r[8];
-    lane_tile_global(Wt, trow, drow, tau, r);
-    return warp_sum_f(sum8(r));
-  };
   // sum of tiles [a, z) in fixed point, one warp
   auto tiles_total = [&](int a, int z) -> unsigned long long {
     unsigned long long tot = 0ull;
@@ -482,23 +527,10 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
       if (sl.unit != cur) {
         cur = sl.unit;
         const DrawDesc d = sdesc[stage];
+        if (cwarp == 0 && lane == 0) cdesc = d;  // for the unit's epilogue
         q = cur / nseg;
         sg = cur - q * nseg;
-        W.mt = d.mt;
-        W.ist = d.ist;
-        W.md = d.md;
-        W.isd = d.isd;
-        W.c2 = d.c2;
-        W.bt0 = 0.f;
-        W.btn = -log2f(d.ist);
-        W.bd = d.kind == 1 ? -log2f(d.isd) : 0.f;
-        W.set_kind(d.kind);
-        W.mask_t = d.kt != 0ull;
-        W.mask_d = d.kind == 1 && d.kd != 0ull;
-        W.vt = W.mask_t ? composite_value(d.kt) : 0.f;
-        W.vd = W.mask_d ? composite_value(d.kd) : 0.f;
-        W.it = uint32_t(composite_index(d.kt));
-        W.id = uint32_t(composite_index(d.kd));
+        W = make_weights(d);
         fast = !W.mask_t && !W.mask_d;
         trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
         drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
@@ -560,144 +592,187 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
     // tiles past the bulk-copied part of the row (last segment), from global memory
     if (run)
       for (int tau = max(ta, nst * kTPS) + cwarp; tau < tz; tau += kDConsumerWarps) {
-        const float tsum = tile_from_global(W, trow, drow, tau);
+        const float tsum = tile_from_global<BF16>(W, trow, drow, tau, V);
         if (lane == 0) ts[tau] = tsum;
       }
     draw_sync();
     if (end || *reinterpret_cast<volatile int*>(&S.cabort)) break;
-    const DrawDesc d = w.draw[q];
-    // With several segments, each keeps its tile sums in the target row's
-    // survivor slot (unused by rows the draw pass serves, past the 8 bytes of
-    // a kept-set threshold), so that the CTA locating the draw reads the
-    // winning segment's sums there instead of streaming its logits again.
-    const bool gstore = nseg > 1 && ntile <= kTileStore;
-    float* gts = reinterpret_cast<float*>(w.cand_raw + size_t(d.tr) * kRawCap) + 16;
-    if (gstore) {
+    // The segment's tile sums (in the target row's survivor slot, unused by
+    // rows the draw pass serves, past the 8 bytes of a kept-set threshold,
+    // when the row's tiles fit there) and its sum, for the locate kernel.
+    if (ntile <= kTileStore) {
+      float* gts = reinterpret_cast<float*>(w.cand_raw + size_t(cdesc.tr) * kRawCap) + 16;
       for (int tau = ta + (tid - 32); tau < tz; tau += kDConsumers) gts[tau] = ts[tau];
-      __threadfence();
     }
-    // the segment's sum; the CTA that completes a draw's last segment locates it
     if (cwarp == 0) {
       const unsigned long long segsum = tiles_total(ta, tz);
-      int last = 1;
-      if (nseg > 1 && lane == 0) {
-        seg_fix[size_t(q) * kMaxSeg + sg] = segsum;
-        __threadfence();
-        last = atomicAdd(&w.seg_cnt[q], 1) == nseg - 1;
-      }
-      if (lane == 0) {
-        S.last = last;
-        S.S = segsum;
-      }
+      if (lane == 0) seg_fix[size_t(q) * kMaxSeg + sg] = segsum;
     }
-    draw_sync();
-    if (!S.last) continue;
-    if (nseg > 1) __threadfence();  // the other segments' sums are read below
-    // total S over the segments
-    if (cwarp == 0) {
-      unsigned long long tot = S.S;
-      if (nseg > 1)
-        tot = warp_sum_u64(lane < nseg ? __ldcg(&seg_fix[size_t(q) * kMaxSeg + lane]) : 0ull);
-      if (lane == 0) {
-        S.S = tot;
-        S.fallback = W.kind == 1 && tot == 0ull;
-      }
-    }
-    draw_sync();
-    int nsegL = nseg;  // segments of the sums the search below walks
-    if (S.fallback) {
-      // residual mass vanished through rounding: draw from p_L, every tile again
-      W.set_kind(2);
-      for (int tau = cwarp; tau < ntile; tau += kDConsumerWarps) {
-        const float tsum = tile_from_global(W, trow, drow, tau);
-        if (lane == 0) ts[tau] = tsum;
-      }
-      draw_sync();
-      if (cwarp == 0) {
-        const unsigned long long tot = tiles_total(0, ntile);
-        if (lane == 0) S.S = tot;
-      }
-      nsegL = 1;
-      draw_sync();
-    }
+    draw_sync();  // tile sums are rewritten by the next unit
+  }
+}
+
+// ------------------------------------------------------------------ locate
+// The draw of each queued request from its segments' sums, after the draw
+// pass: one CTA per draw (persistent over the queue).  Warp 0 reads the
+// segment sums (exact integers, 2^-40 units), forms S and t = floor(u_k S)
+// and finds the segment whose inclusive prefix first exceeds t; the CTA loads
+// that segment's tile sums (stored by the draw pass, else recomputed from the
+// rows), sums them in chunks of 32 tiles side by side, and warp 0 walks the
+// chunk sums, then the chunk's tiles, then the tile's elements (recomputed
+// from the rows) to the first y whose inclusive prefix exceeds t.
+constexpr int kLThreads = 256;
+constexpr int kLWarps = kLThreads / 32;
+
+struct LocateShared {
+  unsigned long long S, R, t;
+  int sstar, fallback;
+};
+
+// Shared memory of the locate kernel: the crossing segment's tile sums (at
+// most every tile of the row), then one fixed-point sum per 32 of them.
+size_t locate_smem_bytes(int V) {
+  const size_t nt = size_t((V + kDTile - 1) / kDTile);
+  return ((sizeof(float) * nt + 15) & ~size_t(15)) + sizeof(unsigned long long) * ((nt + 31) / 32);
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kLThreads) locate_kernel(const Problem P) {
+  using E = Elt<BF16>;
+  extern __shared__ __align__(16) unsigned char lsm[];
+  __shared__ LocateShared L;
+  const Ws& w = P.ws;
+  const int V = P.V;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DrawSegs g = draw_segs<E::kSize>(V, P.n_seg);
+  float* lts = reinterpret_cast<float*>(lsm);
+  unsigned long long* chunk = reinterpret_cast<unsigned long long*>(
+      lsm + ((sizeof(float) * size_t(g.ntile) + 15) & ~size_t(15)));
+  pdl_wait();  // the draw pass's sums
+  const int n_draw = w.hdr->n_draw;
+  // a draw pass that gave up leaves its sums incomplete: nothing is drawn
+  if (w.hdr->err_code == SV_ERR_TIMEOUT) return;
+  const unsigned long long* seg_fix = reinterpret_cast<const unsigned long long*>(w.seg_sum);
+  for (int q = blockIdx.x; q < n_draw; q += gridDim.x) {
+    const DrawDesc d = w.draw[q];
+    Weights W = make_weights(d);
+    const void* trow = static_cast<const char*>(P.target) + d.tr * P.t_stride * E::kSize;
+    const void* drow = d.kind == 1 ? static_cast<const char*>(P.draft) +
+                                         (d.dr - P.Rt) * P.d_stride * E::kSize
+                                   : nullptr;
+    const unsigned long long ufix = (unsigned long long)(d.u * 4294967296.0);  // exact
     // t = floor(u_k S): the draw is the first y whose inclusive prefix
     // exceeds t (for an integer prefix C, C > u S iff C > floor(u S))
-    const unsigned long long Stot = S.S;
-    const unsigned long long ufix = (unsigned long long)(d.u * 4294967296.0);  // exact
-    const unsigned long long t =
-        (__umul64hi(Stot, ufix) << 32) | ((Stot * ufix) >> 32);
-    // the segment whose inclusive prefix first exceeds t (R: the prefix before it)
-    if (cwarp == 0) {
-      int sstar = 0;
-      unsigned long long R = 0ull;
-      if (nsegL > 1) {
-        const unsigned long long v =
-            lane < nseg ? __ldcg(&seg_fix[size_t(q) * kMaxSeg + lane]) : 0ull;
-        const unsigned long long incl = warp_incl_scan_u64(v);
-        const uint32_t hit = __ballot_sync(kFull, lane < nseg && incl > t);
-        const uint32_t pos = __ballot_sync(kFull, lane < nseg && v > 0ull);
-        const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : nseg - 1);
-        sstar = l;
-        R = __shfl_sync(kFull, incl - v, l);
-      }
+    auto floor_uS = [&](unsigned long long Stot) {
+      return (__umul64hi(Stot, ufix) << 32) | ((Stot * ufix) >> 32);
+    };
+    if (warp == 0) {
+      const unsigned long long v =
+          lane < g.nseg ? __ldcg(&seg_fix[size_t(q) * kMaxSeg + lane]) : 0ull;
+      const unsigned long long tot = warp_sum_u64(v);
+      const unsigned long long t = floor_uS(tot);
+      const unsigned long long incl = warp_incl_scan_u64(v);
+      const uint32_t hit = __ballot_sync(kFull, lane < g.nseg && incl > t);
+      const uint32_t pos = __ballot_sync(kFull, lane < g.nseg && v > 0ull);
+      const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : g.nseg - 1);
+      const unsigned long long R = __shfl_sync(kFull, incl - v, l);
       if (lane == 0) {
-        S.tstar = sstar;
-        S.R = R;
+        L.S = tot;
+        L.t = t;
+        L.fallback = W.kind == 1 && tot == 0ull;
+        L.sstar = l;
+        L.R = R;
       }
     }
-    draw_sync();
-    const int sstar = S.tstar;
-    int sa2 = 0, sz2 = ntile;
-    if (nsegL > 1) {
-      seg_tiles(sstar, &sa2, &sz2);
-      if (sstar != sg) {
-        if (gstore) {
-          // that segment's tile sums, as its CTA stored them
-          for (int tau = sa2 + (tid - 32); tau < sz2; tau += kDConsumers)
-            ts[tau] = __ldcg(gts + tau);
-        } else {
-          // that segment's tile sums, recomputed from global memory
-          for (int tau = sa2 + cwarp; tau < sz2; tau += kDConsumerWarps) {
-            const float tsum = tile_from_global(W, trow, drow, tau);
-            if (lane == 0) ts[tau] = tsum;
-          }
+    __syncthreads();
+    int sa, sz;
+    if (L.fallback) {
+      // residual mass vanished through rounding: draw from p_L, every tile
+      W.set_kind(2);
+      sa = 0;
+      sz = g.ntile;
+      for (int tau = warp; tau < sz; tau += kLWarps) {
+        const float ts = tile_from_global<BF16>(W, trow, drow, tau, V);
+        if (lane == 0) lts[tau] = ts;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        unsigned long long tot = 0ull;
+        for (int tau = lane; tau < sz; tau += 32) tot += fixw(lts[tau]);
+        tot = warp_sum_u64(tot);
+        if (lane == 0) {
+          L.S = tot;
+          L.t = floor_uS(tot);
+          L.R = 0ull;
         }
-        draw_sync();
+      }
+    } else {
+      g.tiles(L.sstar, &sa, &sz);
+      if (g.ntile <= kTileStore) {
+        // the segment's tile sums, as the draw pass stored them
+        const float* gts = reinterpret_cast<const float*>(w.cand_raw + size_t(d.tr) * kRawCap) + 16;
+        for (int tau = sa + tid; tau < sz; tau += kLThreads) lts[tau] = __ldcg(gts + tau);
+      } else {
+        // the segment's tile sums, recomputed from the rows
+        for (int tau = sa + warp; tau < sz; tau += kLWarps) {
+          const float ts = tile_from_global<BF16>(W, trow, drow, tau, V);
+          if (lane == 0) lts[tau] = ts;
+        }
       }
     }
-    if (cwarp == 0) {
-      // the tile where the prefix first exceeds t, then the element in it
-      unsigned long long carry = S.R, R = S.R, Rlast = S.R;
-      int tstar = -1, tlast = -1;
-      for (int t0 = sa2; t0 < sz2 && tstar < 0; t0 += 32) {
-        const unsigned long long v = t0 + lane < sz2 ? fixw(ts[t0 + lane]) : 0ull;
+    __syncthreads();
+    // fixed-point sums of 32 tiles each, side by side
+    const int nch = (sz - sa + 31) / 32;
+    for (int c = warp; c < nch; c += kLWarps) {
+      const int tau = sa + c * 32 + lane;
+      const unsigned long long cs = warp_sum_u64(tau < sz ? fixw(lts[tau]) : 0ull);
+      if (lane == 0) chunk[c] = cs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const unsigned long long t = L.t;
+      // the chunk where the prefix first exceeds t, else the last with mass
+      unsigned long long carry = L.R, R = L.R, Rlast = L.R;
+      int cstar = -1, clast = -1;
+      for (int c0 = 0; c0 < nch && cstar < 0; c0 += 32) {
+        const unsigned long long v = c0 + lane < nch ? chunk[c0 + lane] : 0ull;
         const unsigned long long incl = warp_incl_scan_u64(v) + carry;
         const uint32_t pos = __ballot_sync(kFull, v > 0ull);
-        const uint32_t hit = __ballot_sync(kFull, t0 + lane < sz2 && incl > t);
+        const uint32_t hit = __ballot_sync(kFull, c0 + lane < nch && incl > t);
         if (pos) {
           const int l = 31 - __clz(pos);
-          tlast = t0 + l;
+          clast = c0 + l;
           Rlast = __shfl_sync(kFull, incl - v, l);
         }
         if (hit) {
           const int l = __ffs(hit) - 1;
-          tstar = t0 + l;
+          cstar = c0 + l;
           R = __shfl_sync(kFull, incl - v, l);
         }
         carry = __shfl_sync(kFull, incl, 31);
       }
-      if (tstar < 0) {  // t beyond every prefix (rounding): the last tile with mass
-        tstar = tlast;
+      const bool beyond = cstar < 0;  // t beyond every prefix (rounding)
+      if (beyond) {
+        cstar = clast;
         R = Rlast;
       }
       int y = -1;
-      if (tstar >= 0) {
+      if (cstar >= 0) {
+        // the tile in the chunk (the last with mass when beyond)
+        const int tau0 = sa + cstar * 32;
+        const unsigned long long v = tau0 + lane < sz ? fixw(lts[tau0 + lane]) : 0ull;
+        const unsigned long long incl = warp_incl_scan_u64(v) + R;
+        const uint32_t pos = __ballot_sync(kFull, v > 0ull);
+        const uint32_t hit = __ballot_sync(kFull, tau0 + lane < sz && incl > t);
+        const int l = (!beyond && hit) ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+        const int tstar = l >= 0 ? tau0 + l : -1;
+        const unsigned long long Rt = __shfl_sync(kFull, incl - v, max(l, 0));
         // the tile's elements in fixed point; the first one whose inclusive
         // prefix exceeds t, else (the tile's float sum rounded above its
         // elements' fixed-point sum) the last one with mass
-        const int base = tstar * kDTile + lane * 8;
+        const int base = max(tstar, 0) * kDTile + lane * 8;
         float r[8];
-        lane_tile_global(W, trow, drow, tstar, r);
+        lane_tile_global<BF16>(W, trow, drow, max(tstar, 0), V, r);
         unsigned long long wf[8], ls = 0ull;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -706,7 +781,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
         }
         const unsigned long long ex = warp_incl_scan_u64(ls) - ls;
         int ye = INT_MAX, lastp = -1;
-        unsigned long long pre = R + ex;
+        unsigned long long pre = Rt + ex;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           pre += wf[k];
@@ -718,7 +793,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
           ye = min(ye, __shfl_xor_sync(kFull, ye, o));
           lastp = max(lastp, __shfl_xor_sync(kFull, lastp, o));
         }
-        y = ye != INT_MAX ? ye : lastp;
+        y = tstar < 0 ? -1 : ye != INT_MAX ? ye : lastp;
       }
       if (lane == 0) {
         if (y < 0) record_error(w.hdr, SV_ERR_INTERNAL, -1, d.tr);  // no mass found
@@ -729,7 +804,7 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
                      : __int_as_float(0x7fc00000);
       }
     }
-    draw_sync();  // tile sums are rewritten by the next unit
+    __syncthreads();  // L, lts and the chunk sums are rewritten for the next draw
   }
 }
 
@@ -738,6 +813,12 @@ __global__ void __launch_bounds__(kDThreads, 3) draw_pass_kernel(const Problem P
 size_t draw_pass_smem_bytes(int V) {
   return size_t(kDStages) * kDStageBytes + 16 * kDStages +
          sizeof(float) * size_t((V + kDTile - 1) / kDTile);
+}
+
+cudaError_t launch_locate(const Problem& P, bool bf16, int grid, cudaStream_t s) {
+  const size_t smem = locate_smem_bytes(P.V);
+  if (bf16) return launch_after(locate_kernel<true>, grid, kLThreads, smem, s, P);
+  return launch_after(locate_kernel<false>, grid, kLThreads, smem, s, P);
 }
 
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s) {
@@ -754,20 +835,32 @@ cudaError_t draw_configure() {
   cudaError_t e = cudaFuncSetAttribute(draw_pass_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(draw_pass_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(draw_pass_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem);
+  if (e != cudaSuccess) return e;
+  const int lsmem = int(locate_smem_bytes(SV_VOCAB_MAX));
+  e = cudaFuncSetAttribute(locate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           lsmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(locate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              lsmem);
 }
 
-cudaError_t draw_occupancy(int V, int* occ) {
-  int a = 0, b = 0;
-  const size_t smem = draw_pass_smem_bytes(V);
+cudaError_t draw_occupancy(int V, int* occ, int* occ_locate) {
+  int a = 0, b = 0, c = 0, d = 0;
+  const size_t smem = draw_pass_smem_bytes(V), lsmem = locate_smem_bytes(V);
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, draw_pass_kernel<true>,
                                                                 kDThreads, smem);
   if (e == cudaSuccess)
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, draw_pass_kernel<false>, kDThreads,
                                                       smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, locate_kernel<true>, kLThreads, lsmem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, locate_kernel<false>, kLThreads, lsmem);
   if (e != cudaSuccess) return e;
   *occ = max(1, min(a, b));
+  *occ_locate = max(1, min(c, d));
   return cudaSuccess;
 }
 

@@ -28,6 +28,7 @@ constexpr uint64_t kWaitNs = 100ull * 1000 * 1000;       // a wait gives up afte
 constexpr uint32_t kWaitPolls = 1u << 28;                // ... or after this many polls
 constexpr uint64_t kTestWaitNs = 1000ull * 1000;         // the expiring test wait: 1 ms
 constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
+constexpr int kDrawUnitsPerCta = 8;                      // draw-pass units per resident CTA (target)
 
 // Row modes chosen per request by the setup kernel.  kTopk: a filtered row
 // whose top-k is active and at most SV_TOPK_MAX (candidates captured in one
@@ -192,6 +193,7 @@ cudaError_t launch_setup(const Problem& P, cudaStream_t s);
 cudaError_t launch_rowpass(const Problem& P, bool bf16, bool big, int grid, cudaStream_t s);
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_draw(const Problem& P, bool bf16, int grid, cudaStream_t s);
+cudaError_t launch_locate(const Problem& P, bool bf16, int grid, cudaStream_t s);
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s);
 size_t kv_workspace_bytes(int32_t B);
 size_t lmhead_workspace_bytes(int M, int V);
