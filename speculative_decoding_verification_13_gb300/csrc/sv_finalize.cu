@@ -985,20 +985,39 @@ __device__ __forceinline__ void copy_keys_wait() {
 // filtered its row of a wave it starts copying its row of the next wave
 // (survivor keys and count) into its scratch, so that a request going on
 // finds them there.
+// A filtered request's inputs: its parameters, log2(e) / T as chi + clo, the
+// final draw's uniform and (warp 0, lane i) drafted token i.  They depend on
+// the caller's inputs alone, so a CTA reads its first request's before the
+// row pass has finished.
+struct ReqParams {
+  int K;
+  float T, tp, chi, clo, u_last;
+  int x_lane;
+};
+
+__device__ __forceinline__ ReqParams request_params(const Problem& P, int b, int t0, int k) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ReqParams r;
+  r.K = P.top_k[b];
+  r.T = P.temperature[b];
+  r.tp = P.top_p ? P.top_p[b] : 1.0f;
+  log2e_over_t(r.T, &r.chi, &r.clo);
+  r.u_last = warp == 0 ? P.uniforms[t0 + k] : 0.f;
+  r.x_lane = warp == 0 && lane < k ? P.draft_tokens[t0 - b + lane] : -1;
+  return r;
+}
+
 template <bool BF16>
-__device__ void filtered_request(const Problem& P, int b, int t0, int k, WarpScratch* scr,
-                                 PostShared& sh) {
+__device__ void filtered_request(const Problem& P, int b, int t0, int k, const ReqParams& rp,
+                                 WarpScratch* scr, PostShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int d0 = t0 - b;
-  const int K = P.top_k[b];
-  const float T = P.temperature[b];
-  const float tp = P.top_p ? P.top_p[b] : 1.0f;
-  float chi, clo;  // once per request
-  log2e_over_t(T, &chi, &clo);
-  // the final draw's uniform and the drafted tokens (lane i: token i),
-  // fetched while the waves run
-  const float u_last = warp == 0 ? P.uniforms[t0 + k] : 0.f;
-  const int x_lane = warp == 0 && lane < k ? P.draft_tokens[d0 + lane] : -1;
+  const int K = rp.K;
+  const float T = rp.T;
+  const float tp = rp.tp;
+  const float chi = rp.chi, clo = rp.clo;
+  const float u_last = rp.u_last;
+  const int x_lane = rp.x_lane;
   const Ws& w = P.ws;
   int w0 = 0;
   int n_next = -1;  // survivor count of this warp's row of the next wave, being copied
@@ -1078,9 +1097,20 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
   __shared__ PostShared sh;
   const Ws& w = P.ws;
   const int warp = threadIdx.x >> 5;
+  // The job lists and the header counts come from the setup kernel, which has
+  // completed before the row pass let this kernel launch; with the request's
+  // inputs they are read while the row pass finishes.
+  const int gerr = w.hdr->global_err;
+  const int nf = w.hdr->n_filtered, nd = w.hdr->n_decide;
+  int4 job0 = make_int4(0, 0, 0, 0);
+  ReqParams rp0{};
+  if (!gerr && int(blockIdx.x) < nf) {
+    job0 = w.job[blockIdx.x];
+    rp0 = request_params(P, job0.x, job0.z, job0.w);
+  }
   pdl_wait();     // the row pass's results
   pdl_trigger();  // the draw pass may launch; it waits for this kernel
-  if (w.hdr->global_err) {
+  if (gerr) {
     // batch-level data error: every output is -1 (NaN for the probabilities)
     const int64_t stride = int64_t(gridDim.x) * kPostThreads;
     const int64_t i0 = int64_t(blockIdx.x) * kPostThreads + threadIdx.x;
@@ -1090,15 +1120,15 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
       for (int64_t r = i0; r < 2 * P.Rd; r += stride) P.out_pq[r] = nan64();
     return;
   }
-  const int nf = w.hdr->n_filtered, nd = w.hdr->n_decide;
   const int units = nf + (nd + kWarps - 1) / kWarps;
   for (int u = blockIdx.x; u < units; u += gridDim.x) {
     if (u < nf) {
-      const int4 job = w.job[u];
+      const int4 job = u == int(blockIdx.x) ? job0 : w.job[u];
       if (w.req_flag[job.x]) {  // a logit error found by the row pass
         if (warp == 0) fail_request(P, job.x, job.w, job.z, job.z - job.x);
       } else {
-        filtered_request<BF16>(P, job.x, job.z, job.w, scr, sh);
+        const ReqParams rp = u == int(blockIdx.x) ? rp0 : request_params(P, job.x, job.z, job.w);
+        filtered_request<BF16>(P, job.x, job.z, job.w, rp, scr, sh);
       }
       __syncthreads();  // the scratch is reused by the next unit
     } else {

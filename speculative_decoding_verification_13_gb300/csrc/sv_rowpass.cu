@@ -223,10 +223,15 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
     S.tmpcount = 0;
   }
   __syncthreads();
-  // the previous kernel: the setup kernel (its lists and header), or for the
-  // kBig rows the other row pass (which waited for the setup kernel)
+  // The previous kernel: the setup kernel (its lists and header), or for the
+  // kBig rows the other row pass (which waited for the setup kernel).  The
+  // first row pass lets the next kernel launch once the setup kernel is
+  // done; the second one at once, so that the filter kernel can read the
+  // setup kernel's lists and its requests' inputs during the first row
+  // pass's tail (it waits for both row passes before it reads their results).
+  if (BIG) pdl_trigger();
   pdl_wait();
-  pdl_trigger();  // the next kernel may launch; it waits for this one
+  if (!BIG) pdl_trigger();
 
   const int n_active = BIG ? w.hdr->n_big : w.hdr->n_active;
   const int64_t last_row = P.Rt + P.Rd - 1;  // kBig row j is listed at last_row - j
