@@ -65,6 +65,12 @@ struct BigShared {
   unsigned long long bmb[kBandBins + 1], bw[kBandBins + 1];
   unsigned dabove;
   unsigned long long dmass_above, dmass;
+  // the cut of a band whose bins each hold one value: the value, its kept
+  // occurrences (in index order) and their count, the tile holding the last
+  // kept one, the rank of that one in the tile, and its index
+  float fc_v;
+  unsigned fc_m, fc_expect, fc_tile, fc_mr;
+  int fc_idx, fc_ok;
 };
 
 struct BigSync {
@@ -618,247 +624,395 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
   consumer_sync();
   const bool by_value = S.vknown && S.nmixed == 0;
   const float vhi = S.vhi, vlo = S.vlo, vk = S.vk;
-  big_stream<E>(r, ntiles, last_nvec, rowp, tail_start, n_tail,
-                [&](const float* x, int i0, uint32_t vm) {
-    if (bad) return;
-    uint32_t m = 0u;
-#pragma unroll
-    for (int e = 0; e < E::kPerVec; ++e) {
-      const bool in = by_value ? ((x[e] >= vlo && x[e] <= vhi) || x[e] == vk) : in_band(x[e]);
-      m |= (in && ((vm >> e) & 1u)) ? 1u << e : 0u;
-    }
-    if (!__any_sync(0xffffffffu, m != 0u)) return;
-    const int cnt = __popc(m);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int base = 0;
-    if (lane == 31) base = atomicAdd(&S.count, incl);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    int slot = base + incl - cnt;
-#pragma unroll
-    for (int e = 0; e < E::kPerVec; ++e)
-      if ((m >> e) & 1u) {
-        const unsigned long long key = composite_key(x[e], uint32_t(i0 + e));
-        if (slot < kBigCap) keys[slot] = key;
-        ++slot;
-        kmin = key < kmin ? key : kmin;
-        kmax = key > kmax ? key : kmax;
-      }
-  });
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long a = shfl_xor_u64(kmin, o), c = shfl_xor_u64(kmax, o);
-    kmin = a < kmin ? a : kmin;
-    kmax = c > kmax ? c : kmax;
-  }
-  if (lane == 0 && !bad) {
-    atomicMin(&S.minkey, kmin);
-    atomicMax(&S.maxkey, kmax);
-  }
-  consumer_sync();
-  const unsigned long long band_min = S.minkey, band_max = S.maxkey;
-  const int n = S.count;
-  const bool pure = S.nmixed == 0;
-
   unsigned long long kappa = 0ull, Wk = 0ull, Wfin = 0ull;
   int kept = 0;
-  if (!bad && n != S.nband && ctid == 0)
-    flag_request(w, b, SV_ERR_INTERNAL, row);  // the two streams disagree
-  if (!bad && pure && n <= kBigCap && n == S.nband && (!topp_on || phi - plo < kBandBins)) {
+  if (!bad && by_value && (!topp_on || phi - plo < kBandBins)) {
     // ---- every band bin holds one value: the cut follows from the counts
-    // and the value weights, and the kept key from one radix selection over
-    // the band's keys (the r-th largest: r counted from the band's first bin)
-    constexpr uint32_t kSkip = E::kSize == 2 ? kSkipBf16 : kSkipF32;
-    const int first = topp_on ? plo : ck;
-    if (ctid == 0) {
-      // cnt_before / mass_before / value weight of the bins met below
-      S.kept = 0;
-    }
-    consumer_sync();
-    // per-bin facts of the band bins, gathered by their owner threads: slot
-    // bn - plo for the top-p bins, slot kBandBins for a top-k bin apart
-    // from them
+    // and the value weights alone.  The cut's value v and the number m of its
+    // occurrences that are kept are known from the bins; the kept key is that
+    // of the m-th occurrence of v in index order, found by counting v per
+    // tile in one stream and then scanning the one tile that holds it.
     BIG_WALK_BINS({
       const int bn = ctid * BPT + j;
-      if (bn == first) S.cnt_first = cbj;
       const bool in_p = topp_on && bn >= plo && bn <= phi;
-      const bool apart_k = topk_on && bn == ck && !in_p;
-      if (in_p || apart_k) {
-        const int s = in_p ? bn - plo : kBandBins;
-        S.bcnt[s] = c8[j];
-        S.bcb[s] = cbj;
-        S.bmb[s] = mbj;
-        S.bw[s] = c8[j] ? m8[j] / c8[j] : 0ull;  // a single value's weight
+      if (in_p) {
+        const int sl = bn - plo;
+        S.bcnt[sl] = c8[j];
+        S.bcb[sl] = cbj;
+        S.bmb[sl] = mbj;
+        S.bw[sl] = c8[j] ? m8[j] / c8[j] : 0ull;  // a single value's weight
       }
     })
     consumer_sync();
-    unsigned r_k = 0u, r_p = 0u;  // ranks (1-based) in the band of the two cuts
     if (ctid == 0) {
+      S.fc_ok = 1;
+      int cut_bin = -1;
+      unsigned m = 0u;
       unsigned long long W_k = S.total_mass;
       unsigned need = 0u;
-      int sk = -1;
       if (topk_on) {
-        sk = topp_on && ck >= plo && ck <= phi ? ck - plo : kBandBins;
         need = unsigned(K) - S.cnt_ck_before;
-        W_k = S.mass_ck_before + (unsigned long long)need * S.bw[sk];
-        r_k = (S.cnt_ck_before - S.cnt_first) + need;
-        if (topp_on && ck > phi) r_k = (S.cnt_phi_end - S.cnt_first) + need;
+        W_k = S.mass_ck_before + (unsigned long long)need * (S.cnt_ck ? S.mass_ck / S.cnt_ck : 0ull);
+        cut_bin = ck;
+        m = need;
       }
       S.W = W_k;
       S.kept = topk_on ? K : V;
-      S.rk = r_k;
-      S.rp = 0u;
       if (topp_on) {
         const unsigned long long lim = ceil_mul_frac(W_k, tp);
         const int nb = min(phi - plo + 1, kBandBins);
-        for (int s = 0; s < nb; ++s) {
-          const int bn = plo + s;
-          const unsigned c = S.bcnt[s];
+        cut_bin = -1;
+        for (int sl = 0; sl < nb; ++sl) {
+          const int bn = plo + sl;
+          const unsigned c = S.bcnt[sl];
           if (c == 0u) continue;
-          const unsigned long long before = S.bmb[s], wv = S.bw[s];
+          const unsigned long long before = S.bmb[sl], wv = S.bw[sl];
           if (before >= lim) break;  // nothing of this bin is kept
-          // keep element j of the bin while before + j wv < lim
+          // keep occurrence j of the bin's value while before + j wv < lim
           unsigned nk = wv ? unsigned(min((unsigned long long)c, (lim - before + wv - 1) / wv)) : c;
           bool stop = nk < c;
           if (topk_on && bn == ck && nk >= need) {
             nk = need;  // the top-k cut comes first
             stop = true;
           }
-          S.rp = (S.bcb[s] - S.cnt_first) + nk;
+          cut_bin = bn;
+          m = nk;
           S.W = before + (unsigned long long)nk * wv;
-          S.kept = int(S.bcb[s] + nk);
+          S.kept = int(S.bcb[sl] + nk);
           if (stop) break;
         }
-        if (S.rp == 0u) S.kept = -1;  // a band without the crossing
+        if (cut_bin < 0) S.kept = -1;  // a band without the crossing
+      }
+      const unsigned long long h = cut_bin >= 0 ? hm[cut_bin] : 0ull;
+      if (cut_bin < 0 || !(h & kTag) || m == 0u) {
+        S.fc_ok = 0;
+      } else {
+        S.fc_v = __uint_as_float(uint32_t(h));
+        S.fc_m = m;
+        S.fc_expect = hc[cut_bin];
       }
     }
     consumer_sync();
-    r_k = S.rk;
-    r_p = S.rp;
-    Wfin = S.W;
-    kept = S.kept;
-    if (topk_on) {
-      kappa = block_select_kth<kConsumers>(reinterpret_cast<const uint64_t*>(keys), n, int(r_k),
-                                           ctid, hist, sel, BigSync(), kSkip);
-      Wk = Wfin;
+    const bool ok = S.fc_ok != 0;
+    const float fv = S.fc_v;
+    // occurrences of v per tile (the bulk tiles, then the tail as one more)
+    unsigned* tcnt = hc;
+    for (int i = ctid; i <= ntiles; i += kConsumers) tcnt[i] = 0u;
+    consumer_sync();
+    constexpr int kTE = kTileBytes / E::kSize;  // elements per tile
+    big_stream<E>(r, ntiles, last_nvec, rowp, tail_start, n_tail,
+                  [&](const float* x, int i0, uint32_t vm) {
+      if (!ok) return;
+      unsigned c = 0u;
+#pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e) c += ((vm >> e) & 1u) && x[e] == fv ? 1u : 0u;
+      c = __reduce_add_sync(0xffffffffu, c);
+      // a warp's vectors lie in one tile (the tail's elements in the last one)
+      if (lane == 0 && c) atomicAdd(&tcnt[min(i0 / kTE, ntiles)], c);
+    });
+    consumer_sync();
+    if (ok && cwarp == 0) {
+      // the tile holding occurrence m: the first whose inclusive count reaches m
+      unsigned carry = 0u, tstar = ~0u, before = 0u;
+      for (int t0 = 0; t0 <= ntiles; t0 += 32) {
+        const unsigned v = t0 + lane <= ntiles ? tcnt[t0 + lane] : 0u;
+        unsigned incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        incl += carry;
+        const uint32_t hit = __ballot_sync(0xffffffffu, tstar == ~0u && incl >= S.fc_m);
+        if (tstar == ~0u && hit) {
+          const int l = __ffs(hit) - 1;
+          tstar = unsigned(t0 + l);
+          before = __shfl_sync(0xffffffffu, incl - v, l);
+        }
+        carry = __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) {
+        if (carry != S.fc_expect || tstar == ~0u) {
+          S.fc_ok = 0;  // the streams disagree
+        } else {
+          S.fc_tile = tstar;
+          S.fc_mr = S.fc_m - before;
+        }
+      }
     }
-    if (topp_on) {
+    consumer_sync();
+    if (S.fc_ok) {
+      // the tile's elements in index order, a run of consecutive ones per thread
+      const int e0 = int(S.fc_tile) * kTE;
+      const int e1 = min(V, e0 + kTE);
+      constexpr int kRun = kTE / kConsumers;
+      const int a = e0 + ctid * kRun, z = min(e1, a + kRun);
+      unsigned c = 0u;
+      for (int e = a; e < z; ++e) c += E::scalar(rowp, e) == fv ? 1u : 0u;
+      unsigned pre, tot;
+      unsigned long long pm, tm;
+      big_scan(c, 0ull, S, &pre, &pm, &tot, &tm);
+      const unsigned mr = S.fc_mr;
+      if (pre < mr && mr <= pre + c) {
+        unsigned k = pre;
+        for (int e = a; e < z; ++e)
+          if (E::scalar(rowp, e) == fv && ++k == mr) {
+            S.fc_idx = e;
+            break;
+          }
+      }
+      consumer_sync();
+      kappa = composite_key(fv, uint32_t(S.fc_idx));
+      Wfin = S.W;
+      Wk = Wfin;
+      kept = S.kept;
       if (kept < 0) {
         if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
         kept = 0;
+      }
+    } else if (ctid == 0) {
+      flag_request(w, b, SV_ERR_INTERNAL, row);  // the two streams disagree
+    }
+  } else {
+    big_stream<E>(r, ntiles, last_nvec, rowp, tail_start, n_tail,
+                  [&](const float* x, int i0, uint32_t vm) {
+      if (bad) return;
+      uint32_t m = 0u;
+  #pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e) {
+        const bool in = by_value ? ((x[e] >= vlo && x[e] <= vhi) || x[e] == vk) : in_band(x[e]);
+        m |= (in && ((vm >> e) & 1u)) ? 1u << e : 0u;
+      }
+      if (!__any_sync(0xffffffffu, m != 0u)) return;
+      const int cnt = __popc(m);
+      int incl = cnt;
+  #pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&S.count, incl);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int slot = base + incl - cnt;
+  #pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e)
+        if ((m >> e) & 1u) {
+          const unsigned long long key = composite_key(x[e], uint32_t(i0 + e));
+          if (slot < kBigCap) keys[slot] = key;
+          ++slot;
+          kmin = key < kmin ? key : kmin;
+          kmax = key > kmax ? key : kmax;
+        }
+    });
+  #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long a = shfl_xor_u64(kmin, o), c = shfl_xor_u64(kmax, o);
+      kmin = a < kmin ? a : kmin;
+      kmax = c > kmax ? c : kmax;
+    }
+    if (lane == 0 && !bad) {
+      atomicMin(&S.minkey, kmin);
+      atomicMax(&S.maxkey, kmax);
+    }
+    consumer_sync();
+    const unsigned long long band_min = S.minkey, band_max = S.maxkey;
+    const int n = S.count;
+    const bool pure = S.nmixed == 0;
+
+    if (!bad && n != S.nband && ctid == 0)
+      flag_request(w, b, SV_ERR_INTERNAL, row);  // the two streams disagree
+    if (!bad && pure && n <= kBigCap && n == S.nband && (!topp_on || phi - plo < kBandBins)) {
+      // ---- every band bin holds one value: the cut follows from the counts
+      // and the value weights, and the kept key from one radix selection over
+      // the band's keys (the r-th largest: r counted from the band's first bin)
+      constexpr uint32_t kSkip = E::kSize == 2 ? kSkipBf16 : kSkipF32;
+      const int first = topp_on ? plo : ck;
+      if (ctid == 0) {
+        // cnt_before / mass_before / value weight of the bins met below
+        S.kept = 0;
+      }
+      consumer_sync();
+      // per-bin facts of the band bins, gathered by their owner threads: slot
+      // bn - plo for the top-p bins, slot kBandBins for a top-k bin apart
+      // from them
+      BIG_WALK_BINS({
+        const int bn = ctid * BPT + j;
+        if (bn == first) S.cnt_first = cbj;
+        const bool in_p = topp_on && bn >= plo && bn <= phi;
+        const bool apart_k = topk_on && bn == ck && !in_p;
+        if (in_p || apart_k) {
+          const int s = in_p ? bn - plo : kBandBins;
+          S.bcnt[s] = c8[j];
+          S.bcb[s] = cbj;
+          S.bmb[s] = mbj;
+          S.bw[s] = c8[j] ? m8[j] / c8[j] : 0ull;  // a single value's weight
+        }
+      })
+      consumer_sync();
+      unsigned r_k = 0u, r_p = 0u;  // ranks (1-based) in the band of the two cuts
+      if (ctid == 0) {
+        unsigned long long W_k = S.total_mass;
+        unsigned need = 0u;
+        int sk = -1;
+        if (topk_on) {
+          sk = topp_on && ck >= plo && ck <= phi ? ck - plo : kBandBins;
+          need = unsigned(K) - S.cnt_ck_before;
+          W_k = S.mass_ck_before + (unsigned long long)need * S.bw[sk];
+          r_k = (S.cnt_ck_before - S.cnt_first) + need;
+          if (topp_on && ck > phi) r_k = (S.cnt_phi_end - S.cnt_first) + need;
+        }
+        S.W = W_k;
+        S.kept = topk_on ? K : V;
+        S.rk = r_k;
+        S.rp = 0u;
+        if (topp_on) {
+          const unsigned long long lim = ceil_mul_frac(W_k, tp);
+          const int nb = min(phi - plo + 1, kBandBins);
+          for (int s = 0; s < nb; ++s) {
+            const int bn = plo + s;
+            const unsigned c = S.bcnt[s];
+            if (c == 0u) continue;
+            const unsigned long long before = S.bmb[s], wv = S.bw[s];
+            if (before >= lim) break;  // nothing of this bin is kept
+            // keep element j of the bin while before + j wv < lim
+            unsigned nk = wv ? unsigned(min((unsigned long long)c, (lim - before + wv - 1) / wv)) : c;
+            bool stop = nk < c;
+            if (topk_on && bn == ck && nk >= need) {
+              nk = need;  // the top-k cut comes first
+              stop = true;
+            }
+            S.rp = (S.bcb[s] - S.cnt_first) + nk;
+            S.W = before + (unsigned long long)nk * wv;
+            S.kept = int(S.bcb[s] + nk);
+            if (stop) break;
+          }
+          if (S.rp == 0u) S.kept = -1;  // a band without the crossing
+        }
+      }
+      consumer_sync();
+      r_k = S.rk;
+      r_p = S.rp;
+      Wfin = S.W;
+      kept = S.kept;
+      if (topk_on) {
+        kappa = block_select_kth<kConsumers>(reinterpret_cast<const uint64_t*>(keys), n, int(r_k),
+                                             ctid, hist, sel, BigSync(), kSkip);
+        Wk = Wfin;
+      }
+      if (topp_on) {
+        if (kept < 0) {
+          if (ctid == 0) flag_request(w, b, SV_ERR_INTERNAL, row);
+          kept = 0;
+        } else {
+          kappa = block_select_kth<kConsumers>(reinterpret_cast<const uint64_t*>(keys), n,
+                                               int(r_p), ctid, hist, sel, BigSync(), kSkip);
+        }
+      }
+    } else if (!bad && n <= kBigSort && n == S.nband) {
+      // ---- a band bin holds several values: sort the band (descending key)
+      const int P2 = next_pow2(n > 1 ? n : 2);
+      for (int i = n + ctid; i < P2; i += kConsumers) keys[i] = 0ull;  // sorts last
+      consumer_sync();
+      big_sort_desc(keys, P2);
+      const int C = (n + kConsumers - 1) / kConsumers;  // positions per thread
+      const int c0 = min(n, ctid * C), c1 = min(n, c0 + C);
+      unsigned long long cm = 0ull;
+      for (int i = c0; i < c1; ++i) cm += big_wfix(composite_value(keys[i]), M, c2);
+      unsigned dummy_c, dummy_t;
+      unsigned long long pre0, dummy_m;
+      big_scan(0u, cm, S, &dummy_c, &pre0, &dummy_t, &dummy_m);  // mass before c0
+      if (ctid == 0) {
+        S.sk = n;
+        S.nkept = 0;
+      }
+      consumer_sync();
+      if (topk_on) {
+        for (int i = c0; i < c1; ++i)
+          if (bin_of(composite_value(keys[i])) == ck) {
+            atomicMin(&S.sk, i);
+            break;
+          }
+        consumer_sync();
+        const int sk = S.sk;
+        const int pk = sk + int(unsigned(K) - S.cnt_ck_before) - 1;  // the K-th largest
+        unsigned long long pre = pre0;
+        for (int i = c0; i < c1; ++i) {
+          if (i == sk) S.pre_sk = pre;
+          pre += big_wfix(composite_value(keys[i]), M, c2);
+          if (i == pk) {
+            S.pre_pk1 = pre;
+            S.key_k = keys[i];
+          }
+        }
+        consumer_sync();
+        Wk = S.mass_ck_before + (S.pre_pk1 - S.pre_sk);
+        kappa = S.key_k;
+        kept = K;
       } else {
-        kappa = block_select_kth<kConsumers>(reinterpret_cast<const uint64_t*>(keys), n,
-                                             int(r_p), ctid, hist, sel, BigSync(), kSkip);
+        Wk = S.total_mass;
       }
-    }
-  } else if (!bad && n <= kBigSort && n == S.nband) {
-    // ---- a band bin holds several values: sort the band (descending key)
-    const int P2 = next_pow2(n > 1 ? n : 2);
-    for (int i = n + ctid; i < P2; i += kConsumers) keys[i] = 0ull;  // sorts last
-    consumer_sync();
-    big_sort_desc(keys, P2);
-    const int C = (n + kConsumers - 1) / kConsumers;  // positions per thread
-    const int c0 = min(n, ctid * C), c1 = min(n, c0 + C);
-    unsigned long long cm = 0ull;
-    for (int i = c0; i < c1; ++i) cm += big_wfix(composite_value(keys[i]), M, c2);
-    unsigned dummy_c, dummy_t;
-    unsigned long long pre0, dummy_m;
-    big_scan(0u, cm, S, &dummy_c, &pre0, &dummy_t, &dummy_m);  // mass before c0
-    if (ctid == 0) {
-      S.sk = n;
-      S.nkept = 0;
-    }
-    consumer_sync();
-    if (topk_on) {
-      for (int i = c0; i < c1; ++i)
-        if (bin_of(composite_value(keys[i])) == ck) {
-          atomicMin(&S.sk, i);
-          break;
+      Wfin = Wk;
+      if (topp_on) {
+        // keep j while the mass before it is below ceil(top_p * W_k) (and j is
+        // within the top k): a prefix of the band's first bins
+        const unsigned long long lim = ceil_mul_frac(Wk, tp);
+        const unsigned long long kfloor = kappa;
+        unsigned long long pre = pre0;
+        int nk = 0;
+        for (int i = c0; i < c1; ++i) {
+          const unsigned long long key = keys[i];
+          const float v = composite_value(key);
+          if (bin_of(v) <= phi && S.mass_p_before + pre < lim && key >= kfloor) ++nk;
+          pre += big_wfix(v, M, c2);
         }
-      consumer_sync();
-      const int sk = S.sk;
-      const int pk = sk + int(unsigned(K) - S.cnt_ck_before) - 1;  // the K-th largest
-      unsigned long long pre = pre0;
-      for (int i = c0; i < c1; ++i) {
-        if (i == sk) S.pre_sk = pre;
-        pre += big_wfix(composite_value(keys[i]), M, c2);
-        if (i == pk) {
-          S.pre_pk1 = pre;
-          S.key_k = keys[i];
+        if (nk) atomicAdd(&S.nkept, nk);
+        consumer_sync();
+        const int istar = S.nkept - 1;
+        pre = pre0;
+        for (int i = c0; i < c1; ++i) {
+          const unsigned long long key = keys[i];
+          const unsigned long long wf = big_wfix(composite_value(key), M, c2);
+          if (i == istar) {
+            S.key = key;
+            S.W = S.mass_p_before + pre + wf;
+          }
+          pre += wf;
+        }
+        consumer_sync();
+        if (istar >= 0) {
+          kappa = S.key;
+          Wfin = S.W;
+          kept = int(S.cnt_p_before) + istar + 1;
+        } else if (ctid == 0) {
+          flag_request(w, b, SV_ERR_INTERNAL, row);  // a band without the crossing
         }
       }
-      consumer_sync();
-      Wk = S.mass_ck_before + (S.pre_pk1 - S.pre_sk);
-      kappa = S.key_k;
-      kept = K;
-    } else {
+    } else if (!bad && n == S.nband) {
+      // ---- exact radix selection over the band, from global memory
+      unsigned* xc = reinterpret_cast<unsigned*>(work);
+      unsigned long long* xm = reinterpret_cast<unsigned long long*>(work + 1024);
+      kappa = 0ull;
       Wk = S.total_mass;
-    }
-    Wfin = Wk;
-    if (topp_on) {
-      // keep j while the mass before it is below ceil(top_p * W_k) (and j is
-      // within the top k): a prefix of the band's first bins
-      const unsigned long long lim = ceil_mul_frac(Wk, tp);
-      const unsigned long long kfloor = kappa;
-      unsigned long long pre = pre0;
-      int nk = 0;
-      for (int i = c0; i < c1; ++i) {
-        const unsigned long long key = keys[i];
-        const float v = composite_value(key);
-        if (bin_of(v) <= phi && S.mass_p_before + pre < lim && key >= kfloor) ++nk;
-        pre += big_wfix(v, M, c2);
+      kept = V;
+      if (topk_on) {
+        auto in_k = [&](float x) { return bin_of(x) == ck; };
+        kappa = big_radix<E>(rowp, V, M, c2, false, unsigned(K) - S.cnt_ck_before, 0ull, 0ull,
+                             S.cnt_ck_before, S.mass_ck_before, band_min, band_max, in_k, xc, xm,
+                             S, &Wk, &kept);
       }
-      if (nk) atomicAdd(&S.nkept, nk);
-      consumer_sync();
-      const int istar = S.nkept - 1;
-      pre = pre0;
-      for (int i = c0; i < c1; ++i) {
-        const unsigned long long key = keys[i];
-        const unsigned long long wf = big_wfix(composite_value(key), M, c2);
-        if (i == istar) {
-          S.key = key;
-          S.W = S.mass_p_before + pre + wf;
-        }
-        pre += wf;
+      Wfin = Wk;
+      if (topp_on) {
+        auto in_p = [&](float x) {
+          const int bn = bin_of(x);
+          return bn >= plo && bn <= phi;
+        };
+        kappa = big_radix<E>(rowp, V, M, c2, true, 0u, ceil_mul_frac(Wk, tp), kappa,
+                             S.cnt_p_before, S.mass_p_before, band_min, band_max, in_p, xc, xm, S,
+                             &Wfin, &kept);
       }
-      consumer_sync();
-      if (istar >= 0) {
-        kappa = S.key;
-        Wfin = S.W;
-        kept = int(S.cnt_p_before) + istar + 1;
-      } else if (ctid == 0) {
-        flag_request(w, b, SV_ERR_INTERNAL, row);  // a band without the crossing
-      }
-    }
-  } else if (!bad && n == S.nband) {
-    // ---- exact radix selection over the band, from global memory
-    unsigned* xc = reinterpret_cast<unsigned*>(work);
-    unsigned long long* xm = reinterpret_cast<unsigned long long*>(work + 1024);
-    kappa = 0ull;
-    Wk = S.total_mass;
-    kept = V;
-    if (topk_on) {
-      auto in_k = [&](float x) { return bin_of(x) == ck; };
-      kappa = big_radix<E>(rowp, V, M, c2, false, unsigned(K) - S.cnt_ck_before, 0ull, 0ull,
-                           S.cnt_ck_before, S.mass_ck_before, band_min, band_max, in_k, xc, xm,
-                           S, &Wk, &kept);
-    }
-    Wfin = Wk;
-    if (topp_on) {
-      auto in_p = [&](float x) {
-        const int bn = bin_of(x);
-        return bn >= plo && bn <= phi;
-      };
-      kappa = big_radix<E>(rowp, V, M, c2, true, 0u, ceil_mul_frac(Wk, tp), kappa,
-                           S.cnt_p_before, S.mass_p_before, band_min, band_max, in_p, xc, xm, S,
-                           &Wfin, &kept);
     }
   }
-
   if (ctid == 0) {
     double pg = __longlong_as_double(0x7ff8000000000000LL);
     const int gx = ent.gx;
