@@ -459,10 +459,12 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
   // 2^(E - 8) for bf16, 2^(E - 24) for f32; the bin width is 1 / cs).
   const int ethr = int(floorf(127.0f + float(E::kSize == 2 ? 8 : 24) + 1.0f - log2f(cs) +
                               1e-3f)) + 1;
+  // |x| >= thr_abs iff the exponent of x reaches ethr
+  const float thr_abs = ethr <= 0 ? 0.0f : (ethr >= 255 ? INFINITY : __int_as_float(ethr << 23));
 
   // ---- B: counts per bin; masses per bin, in fixed point: a single-value
-  // bin records its value (its mass is the count times that value's weight),
-  // any other bin sums its elements' weights
+  // bin's mass is its count times its value's weight (the value is recovered
+  // from the bin below), any other bin sums its elements' weights
   for (int i = ctid; i < kBigBins; i += kConsumers) {
     hc[i] = 0u;
     hm[i] = 0ull;
@@ -476,10 +478,7 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
       if (!((vm >> e) & 1u)) continue;
       const int bn = bin_of(x[e]);
       atomicAdd(&hc[bn], 1u);
-      const int ef = int((__float_as_uint(x[e]) >> 23) & 0xffu);
-      if (bn < kBigBins - 2 && ef >= ethr) {
-        hm[bn] = kTag | __float_as_uint(x[e]);  // every writer stores the same value
-      } else {
+      if (bn >= kBigBins - 2 || !(fabsf(x[e]) >= thr_abs)) {
         const unsigned long long wf = big_wfix(x[e], M, c2);
         if (wf) atomicAdd(&hm[bn], wf);
       }
@@ -493,10 +492,29 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
   unsigned long long m8[BPT];
   unsigned lc = 0u, pure_mask = 0u;
   unsigned long long lm = 0ull;
+  const double inv_cs = 1.0 / double(cs);  // the bin width, for the bins' centres
 #pragma unroll
   for (int j = 0; j < BPT; ++j) {
-    c8[j] = hc[ctid * BPT + j];
-    const unsigned long long h = hm[ctid * BPT + j];
+    const int bn = ctid * BPT + j;
+    c8[j] = hc[bn];
+    unsigned long long h = hm[bn];
+    if (c8[j] > 0u && h == 0ull && bn < kBigBins - 2) {
+      // A bin whose elements reach ethr holds one value, the representable
+      // value nearest the bin's centre M - bn / cs (any other lies at least
+      // 1.5 bin widths from it); its elements added no mass.  Its value is
+      // recorded as the bin's tag.
+      const float vc = float(fma(-double(bn), inv_cs, double(M)));
+      float v = vc;
+      if (E::kSize == 2) {
+        uint32_t u = __float_as_uint(vc);
+        u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;  // to bf16, nearest even
+        v = __uint_as_float(u);
+      }
+      if (fabsf(v) >= thr_abs && bin_of(v) == bn) {
+        h = kTag | __float_as_uint(v);
+        hm[bn] = h;
+      }
+    }
     if (h & kTag) {
       m8[j] = (unsigned long long)c8[j] * big_wfix(__uint_as_float(uint32_t(h)), M, c2);
       pure_mask |= 1u << j;
