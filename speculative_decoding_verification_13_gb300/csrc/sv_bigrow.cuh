@@ -763,21 +763,40 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
       // the tile's elements in index order, a run of consecutive ones per thread
       const int e0 = int(S.fc_tile) * kTE;
       const int e1 = min(V, e0 + kTE);
-      constexpr int kRun = kTE / kConsumers;
+      constexpr int kRun = kTE / kConsumers;  // 64 bytes: four 16-byte vectors
+      constexpr int kVec = kRun / E::kPerVec;
+      static_assert(kVec == 4, "a thread's run is four vectors");
       const int a = e0 + ctid * kRun, z = min(e1, a + kRun);
-      unsigned c = 0u;
-      for (int e = a; e < z; ++e) c += E::scalar(rowp, e) == fv ? 1u : 0u;
+      // the run's match mask (bit i: element a + i), from four vector loads
+      // when the run lies whole inside the row
+      uint32_t mm = 0u;
+      if (z - a == kRun) {
+        const uint4* vp = reinterpret_cast<const uint4*>(static_cast<const char*>(rowp) +
+                                                         size_t(a) * E::kSize);
+        uint4 q[kVec];
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) q[i] = __ldcg(vp + i);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+          float x[E::kPerVec];
+          E::decode(q[i], x);
+#pragma unroll
+          for (int e = 0; e < E::kPerVec; ++e)
+            mm |= x[e] == fv ? 1u << (i * E::kPerVec + e) : 0u;
+        }
+      } else {
+        for (int e = a; e < z; ++e) mm |= E::scalar(rowp, e) == fv ? 1u << (e - a) : 0u;
+      }
+      const unsigned c = __popc(mm);
       unsigned pre, tot;
       unsigned long long pm, tm;
       big_scan(c, 0ull, S, &pre, &pm, &tot, &tm);
       const unsigned mr = S.fc_mr;
       if (pre < mr && mr <= pre + c) {
-        unsigned k = pre;
-        for (int e = a; e < z; ++e)
-          if (E::scalar(rowp, e) == fv && ++k == mr) {
-            S.fc_idx = e;
-            break;
-          }
+        // the (mr - pre)-th set bit of the mask
+        uint32_t m2 = mm;
+        for (unsigned k = pre + 1; k < mr; ++k) m2 &= m2 - 1u;
+        S.fc_idx = a + __ffs(m2) - 1;
       }
       consumer_sync();
       kappa = composite_key(fv, uint32_t(S.fc_idx));
