@@ -287,9 +287,10 @@ def measure_e2e(args, batch, v, acc, tok, stream, dev, pg):
     import torch
     ws = pg.get_world_size() if pg else 1
     B, Rt = batch.batch, batch.target_rows
-    host = {k: getattr(batch, k).to("cpu").pin_memory() for k in
-            ("target", "draft", "draft_tokens", "k_per_req", "temperature", "top_k", "top_p",
-             "uniforms")}
+    filtered = batch.filters()[0] is not None
+    names = ("target", "draft", "draft_tokens", "k_per_req", "temperature", "uniforms") + \
+        (("top_k", "top_p") if filtered else ())
+    host = {k: getattr(batch, k).to("cpu").pin_memory() for k in names}
     dbuf = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
     acc_h = torch.empty(B, dtype=torch.int32).pin_memory()
     tok_h = torch.empty(Rt, dtype=torch.int32).pin_memory()
@@ -300,7 +301,7 @@ def measure_e2e(args, batch, v, acc, tok, stream, dev, pg):
         for k_, t in host.items():
             dbuf[k_].copy_(t, non_blocking=True)
         a, o = v(dbuf["target"], dbuf["draft"], dbuf["draft_tokens"], dbuf["k_per_req"],
-                 dbuf["temperature"], dbuf["uniforms"], dbuf["top_k"], dbuf["top_p"],
+                 dbuf["temperature"], dbuf["uniforms"], dbuf.get("top_k"), dbuf.get("top_p"),
                  out_accept_len=acc, out_tokens=tok)
         acc_h.copy_(a, non_blocking=True)
         tok_h.copy_(o, non_blocking=True)
@@ -348,7 +349,8 @@ def run_sampler(args, ws, rank, local):
         pg.barrier()
     sv.load_library()
     batch = workloads.make_batch(args.config, device=dev, seed_offset=rank, batch=args.batch)
-    x, k, T, tk, tp = batch.draft, batch.k_per_req, batch.temperature, batch.top_k, batch.top_p
+    x, k, T = batch.draft, batch.k_per_req, batch.temperature
+    tk, tp = batch.filters()
     R, V = x.shape
     g = torch.Generator(device=dev)
     g.manual_seed(1400 + rank)
@@ -455,7 +457,7 @@ def run_sampler(args, ws, rank, local):
                      "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
                      "launch_ms": rowpass_ms, "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": (6 if tk is not None else 5) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -809,8 +811,9 @@ def main():
     acc = torch.empty(B, dtype=torch.int32, device=dev)
     tok = torch.empty(Rt, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    top_k, top_p = batch.filters()
     call = lambda evs=None: v(batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
-                              batch.temperature, batch.uniforms, batch.top_k, batch.top_p,
+                              batch.temperature, batch.uniforms, top_k, top_p,
                               out_accept_len=acc, out_tokens=tok, rowpass_events=evs)
 
     clocks = ClockSampler(local) if rank == 0 else None
@@ -880,7 +883,7 @@ def main():
     if ws == 1 and not args.no_parity:
         pq = torch.full((max(Rd, 1), 2), float("nan"), dtype=torch.float64, device=dev)
         a1, t1 = v(batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
-                   batch.temperature, batch.uniforms, batch.top_k, batch.top_p, out_pq=pq)
+                   batch.temperature, batch.uniforms, top_k, top_p, out_pq=pq)
         parity = parity_vs_oracle(batch, a1, t1, pq)
     dtype = "bf16" if batch.target.dtype == torch.bfloat16 else "f32"
     line = {
@@ -918,7 +921,7 @@ def main():
                      "bytes_per_launch": bytes_req, "launch_ms": rowpass_ms,
                      "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": 6 * args.steps,
+        "gpu_launches": (6 if top_k is not None else 5) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "parity": parity,

@@ -136,7 +136,9 @@ size_t spec_verify_workspace_size(int32_t batch, int64_t target_rows, int64_t dr
  *   top_k          [B] int32 or NULL; 0 or >= V switches top-k off; any
  *                  value in [1, V) is supported
  *   top_p          [B] float or NULL; 1 switches top-p off; (0, 1]; top-k
- *                  and top-p switch on and off independently
+ *                  and top-p switch on and off independently; with both
+ *                  NULL no row is filtered and the call launches one
+ *                  kernel fewer (the row pass over threshold-filtered rows)
  *   uniforms       [R_t] float in [0, 1)
  *   out_accept_len [B] int32 (L, or -1 on a data error)
  *   out_tokens     [R_t] int32

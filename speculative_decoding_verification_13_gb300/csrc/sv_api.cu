@@ -148,9 +148,12 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
     return SV_ERR_CUDA;
   // every row but those filtered by a kept-set threshold (top-p alone, large
   // top-k), then those: the second launch's CTAs become resident in the
-  // first one's tail, so that it costs little when it has no rows
+  // first one's tail, so that it costs little when it has no rows; without
+  // top_k and top_p arrays no row can need it, and it is not launched
+  const bool threshold_rows = top_k != nullptr || top_p != nullptr;
   if (grid > 0 && (launch_rowpass(P, t.dtype == SV_BF16, false, grid, s) != cudaSuccess ||
-                   launch_rowpass(P, t.dtype == SV_BF16, true, grid, s) != cudaSuccess))
+                   (threshold_rows &&
+                    launch_rowpass(P, t.dtype == SV_BF16, true, grid, s) != cudaSuccess)))
     return SV_ERR_CUDA;
   if (options && options->event_rowpass_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)
@@ -237,8 +240,10 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   if (options && options->event_rowpass_begin &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_begin), s) != cudaSuccess)
     return SV_ERR_CUDA;
+  const bool threshold_rows = top_k != nullptr || top_p != nullptr;
   if (launch_rowpass(P, bf16, false, int(rows < ctas ? rows : ctas), s) != cudaSuccess ||
-      launch_rowpass(P, bf16, true, int(rows < ctas ? rows : ctas), s) != cudaSuccess)
+      (threshold_rows &&
+       launch_rowpass(P, bf16, true, int(rows < ctas ? rows : ctas), s) != cudaSuccess))
     return SV_ERR_CUDA;
   if (options && options->event_rowpass_end &&
       cudaEventRecord(static_cast<cudaEvent_t>(options->event_rowpass_end), s) != cudaSuccess)

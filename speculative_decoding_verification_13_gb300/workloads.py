@@ -64,6 +64,14 @@ class Batch:
     def draft_rows(self) -> int:
         return int(self.draft.shape[0])
 
+    def filters(self):
+        """(top_k, top_p) for a call: None for both when the workload has no
+        filter (its arrays hold only the switched-off values), which tells
+        the library that no row can need the kept-set threshold pass."""
+        if self.meta.get("filtered", True):
+            return self.top_k, self.top_p
+        return None, None
+
     def logit_bytes(self) -> int:
         es = self.target.element_size()
         return (self.target_rows + self.draft_rows) * self.vocab * es
@@ -227,7 +235,8 @@ def make_batch_from_params(name, k_list, temps, sigmas, V, dtype, seed, device="
     else:
         tokens = torch.zeros(0, dtype=torch.int32, device=device)
     uniforms = torch.rand(Rt, generator=g, device=device)
-    meta = dict(seed=seed, sigmas=sig.tolist() if B <= 64 else None, V=V)
+    meta = dict(seed=seed, sigmas=sig.tolist() if B <= 64 else None, V=V,
+                filtered=top_k is not None or top_p is not None)
     return Batch(name, target, draft, tokens, k.to(device), T.to(device), tk.to(device),
                  tp.to(device), uniforms, meta)
 

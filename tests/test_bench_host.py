@@ -64,6 +64,17 @@ def test_required_bytes_skip_greedy_draft_rows():
     assert nbytes == rows * 64 * 4
 
 
+def test_unfiltered_workloads_pass_no_filter_arrays():
+    """Configs without a filter call the library with top_k = top_p = None
+    (one launch fewer); filtered ones pass their arrays."""
+    from speculative_decoding_verification_13_gb300 import workloads
+    b = workloads.make_batch("c1", "t1")
+    assert b.filters() == (None, None)
+    assert int(b.top_k.abs().sum()) == 0 and bool((b.top_p == 1).all())
+    f = workloads.make_batch("c4", batch=2).filters()
+    assert f[0] is not None and f[1] is not None
+
+
 def bench_dtype():
     import torch
     return torch.float32

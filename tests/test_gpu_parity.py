@@ -102,6 +102,20 @@ def test_softmax_statistics_match_torch_logsumexp():
     assert float(rel.max()) < 1e-6
 
 
+def test_no_filter_arrays_equal_switched_off_filters():
+    """top_k = top_p = NULL (no threshold row pass is launched) gives the
+    same results as arrays of switched-off values."""
+    for cfg, var in (("c3", "s1"), ("c5", None), ("c1", "t1")):
+        batch = W.make_batch(cfg, var, device=DEV, batch=None if cfg == "c1" else 24)
+        v = sv.Verifier(DEV)
+        args = (batch.target, batch.draft, batch.draft_tokens, batch.k_per_req,
+                batch.temperature, batch.uniforms)
+        a0, t0 = (x.cpu() for x in v(*args, batch.top_k, batch.top_p))
+        a1, t1 = (x.cpu() for x in v(*args, None, None))
+        assert v.error()[0] == 0
+        assert torch.equal(a0, a1) and torch.equal(t0, t1), cfg
+
+
 def test_filtered_kept_sets_match_oracle():
     batch = W.make_batch("c4", device=DEV, batch=16)
     v = sv.Verifier(DEV)
