@@ -515,41 +515,45 @@ def run_kv(args, ws, rank, local):
     cache, spec = caches[0], specs[0]
     tokens = int((acc.clamp(min=-1) + 1).sum())
     bytes_per_step = 2 * tokens * layers * 2 * E * 2      # read and write
-    kv_len = n0.clone()
+    # one kv_len array per call of a graph (KV_GRAPH_STEPS calls), all reset
+    # to the starting lengths by one copy before the calls
+    n0s = n0.repeat(KV_GRAPH_STEPS, 1)
+    kv_lens = n0s.clone()
     stream = torch.cuda.current_stream(dev)
-    it = [0]
 
-    def step():
-        r = it[0] % KV_REPLICAS
-        it[0] += 1
-        kv_len.copy_(n0)
-        sv.kv_commit(caches[r], specs[r], acc, batch.k_per_req, kv_len, table)
+    def call(i):
+        sv.kv_commit(caches[i % KV_REPLICAS], specs[i % KV_REPLICAS], acc, batch.k_per_req,
+                     kv_lens[i], table)
+
+    def calls():
+        kv_lens.copy_(n0s)
+        for i in range(KV_GRAPH_STEPS):
+            call(i)
     clocks = ClockSampler(local) if rank == 0 else None
-    for _ in range(args.warmup):
-        step()
+    for _ in range(max(1, args.warmup // KV_GRAPH_STEPS)):
+        calls()
     torch.cuda.synchronize(dev)
     if sv.kv_commit_error(device=dev)[0] != 0:
         raise RuntimeError("KV commit data error during warm-up")
     # the host cost of one call through the Python binding (argument checks
     # and marshalling), which is of the order of the GPU's own time here
     t0 = time.perf_counter()
-    for _ in range(50):
-        step()
-    host_us = (time.perf_counter() - t0) / 50 * 1e6
+    for _ in range(3):
+        calls()
+    host_us = (time.perf_counter() - t0) / (3 * KV_GRAPH_STEPS) * 1e6
     torch.cuda.synchronize(dev)
-    # the timed steps replay a CUDA graph of KV_GRAPH_STEPS calls, so that
-    # the GPU's time is measured rather than the host's issue rate
+    # the timed steps replay a CUDA graph of KV_GRAPH_STEPS calls (and the one
+    # kv_len reset), so that the GPU's time is measured rather than the host's
+    # issue rate
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        for _ in range(3):
-            step()
+        calls()
     stream.wait_stream(side)
     torch.cuda.synchronize(dev)
     with torch.cuda.graph(graph):
-        for _ in range(KV_GRAPH_STEPS):
-            step()
+        calls()
     replays = max(1, (args.steps + KV_GRAPH_STEPS - 1) // KV_GRAPH_STEPS)
     graph.replay()
     torch.cuda.synchronize(dev)
@@ -596,9 +600,9 @@ def run_kv(args, ws, rank, local):
         "steps": timed_steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (accept lengths from verifying the seeded bench batch; random K/V)",
-        "timing": f"CUDA graph of {KV_GRAPH_STEPS} calls (kv_len reset + spec_kv_commit), "
-                  f"replayed {replays} times; host cost of one call through the Python "
-                  f"binding {host_us:.1f} us",
+        "timing": f"CUDA graph of {KV_GRAPH_STEPS} spec_kv_commit calls (one kv_len array "
+                  f"each, all reset by one copy per graph), replayed {replays} times; host "
+                  f"cost of one call through the Python binding {host_us:.1f} us",
         "config": {"workload": f"B={B} commits after k=15 verification, {tokens} tokens, "
                                f"{layers} layers x K,V x {E} bf16 per token, {S}-token pages",
                    "tokens_per_step": tokens, "bytes_per_step": bytes_per_step,
@@ -608,7 +612,7 @@ def run_kv(args, ws, rank, local):
         "roofline": {"bound": "hbm", "kernel": "kv_copy_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": peak_src, "bytes_per_launch": bytes_per_step,
-                     "note": "timed over whole calls (kv_len reset, validation, copy)"},
+                     "note": "timed over whole calls (validation, copy, kv_len update)"},
         "e2e": None,
         "gpu_launches": 2 * timed_steps,
         "clocks": clk,
