@@ -473,6 +473,28 @@ __device__ __forceinline__ void big_row(const Problem& P, const BigRing& r, BigS
   big_stream<E>(r, ntiles, last_nvec, rowp, tail_start, n_tail,
                 [&](const float* x, int, uint32_t vm) {
     if (bad) return;
+    constexpr uint32_t kAllE = (1u << E::kPerVec) - 1u;
+    if (vm == kAllE) {
+      // a whole vector: the bins first, then the counts, then the rare masses
+      int bn[E::kPerVec];
+#pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e) bn[e] = bin_of(x[e]);
+#pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e) atomicAdd(&hc[bn[e]], 1u);
+      uint32_t mixed = 0u;
+#pragma unroll
+      for (int e = 0; e < E::kPerVec; ++e)
+        mixed |= (bn[e] >= kBigBins - 2 || !(fabsf(x[e]) >= thr_abs)) ? 1u << e : 0u;
+      if (mixed) {
+#pragma unroll
+        for (int e = 0; e < E::kPerVec; ++e)
+          if ((mixed >> e) & 1u) {
+            const unsigned long long wf = big_wfix(x[e], M, c2);
+            if (wf) atomicAdd(&hm[bn[e]], wf);
+          }
+      }
+      return;
+    }
 #pragma unroll
     for (int e = 0; e < E::kPerVec; ++e) {
       if (!((vm >> e) & 1u)) continue;

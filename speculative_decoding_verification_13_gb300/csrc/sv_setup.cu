@@ -98,6 +98,10 @@ __global__ void __launch_bounds__(kSetupThreads) setup_kernel(const Problem P) {
   const Ws& w = P.ws;
   __shared__ int s_bad;
   __shared__ ReqRows s_req[kSetupThreads];
+  // launched as a dependent of whatever the stream ran before (the previous
+  // call's last kernel, or the kernel that produced the inputs): nothing is
+  // read or written before that has completed
+  pdl_wait();
   pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
   // Every CTA forms the same offsets, modes and scans; CTA 0 alone writes the
   // header, the offsets, the flags and the job lists, and each CTA writes its
@@ -283,6 +287,10 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
   const Ws& w = P.ws;
   __shared__ int s_bad;
   __shared__ ReqRows s_req[kSetupThreads];
+  // launched as a dependent of whatever the stream ran before (the previous
+  // call's last kernel, or the kernel that produced the inputs): nothing is
+  // read or written before that has completed
+  pdl_wait();
   pdl_trigger();  // the row pass may launch and set up; it waits for this kernel
   // As in the verifier's setup: CTA 0 writes the header, offsets, flags and
   // the outputs of failed requests; every CTA writes its share of the row
@@ -405,13 +413,11 @@ __global__ void __launch_bounds__(kSetupThreads) sample_setup_kernel(const Probl
 int setup_grid(int64_t B) { return B <= kSetupThreads ? kSetupCtas : 1; }
 
 cudaError_t launch_sample_setup(const Problem& P, cudaStream_t s) {
-  sample_setup_kernel<<<setup_grid(P.B), kSetupThreads, 0, s>>>(P);
-  return cudaGetLastError();
+  return launch_after(sample_setup_kernel, setup_grid(P.B), kSetupThreads, 0, s, P);
 }
 
 cudaError_t launch_setup(const Problem& P, cudaStream_t s) {
-  setup_kernel<<<setup_grid(P.B), kSetupThreads, 0, s>>>(P);
-  return cudaGetLastError();
+  return launch_after(setup_kernel, setup_grid(P.B), kSetupThreads, 0, s, P);
 }
 
 }  // namespace sv
