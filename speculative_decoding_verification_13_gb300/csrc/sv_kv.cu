@@ -70,6 +70,9 @@ __device__ int kv_block_scan(int v, int* total) {
 }
 
 __global__ void __launch_bounds__(kKvThreads) kv_validate_kernel(const KvProblem Q) {
+  // launched as a dependent of whatever the stream ran before: nothing is
+  // read or written before that has completed
+  pdl_wait();
   pdl_trigger();  // the copy kernel may launch; it waits for this one
   if (threadIdx.x == 0) {
     Q.hdr->err_code = 0;
@@ -181,8 +184,17 @@ cudaError_t launch_kv_commit(void* cache, const void* spec, int64_t num_pages, i
   Q.start = reinterpret_cast<int32_t*>(w + o);
   o = align256(o + sizeof(int32_t) * size_t(B > 0 ? B : 1));
   Q.tokens = reinterpret_cast<int2*>(w + o);
-  kv_validate_kernel<<<1, kKvThreads, 0, s>>>(Q);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t vc = {};
+  vc.gridDim = dim3(1);
+  vc.blockDim = dim3(kKvThreads);
+  vc.dynamicSmemBytes = 0;
+  vc.stream = s;
+  cudaLaunchAttribute va[1];
+  va[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  va[0].val.programmaticStreamSerializationAllowed = 1;
+  vc.attrs = va;
+  vc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&vc, kv_validate_kernel, Q);
   if (e != cudaSuccess) return e;
   // enough warps for every entry of the largest commit, at most 8 CTAs per SM
   const int64_t items = int64_t(B) * (spec_slots < SV_MAX_K + 1 ? spec_slots : SV_MAX_K + 1) *
