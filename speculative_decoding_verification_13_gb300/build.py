@@ -1,6 +1,6 @@
 """In-tree build of libspecverify.so for sm_103a (nvcc, no cmake).
 
-The four translation units compile in parallel, then link into
+The translation units compile in parallel, then link into
 ``_lib/libspecverify.so`` against the shared CUDA runtime.
 """
 

@@ -82,3 +82,21 @@ def test_empty_batch():
     sv.kv_commit(cache, spec, e, e, e.clone(), torch.zeros(0, 2, dtype=torch.int32, device=DEV))
     torch.cuda.synchronize()
     assert (cache == 0).all()
+
+
+@pytest.mark.parametrize("B", [1025, 4097])
+def test_batches_past_one_validation_round(B):
+    # the validation CTA takes 1024 requests a round: its scan carries the
+    # token offsets from round to round
+    code, st = run_both(*case(B, B, 1, 8, 4, 15))
+    assert code == 0 and (st == 0).all()
+
+
+def test_calls_of_several_sizes_reuse_one_workspace():
+    # a workspace sized for the largest batch first, then smaller batches on
+    # the same workspace: nothing of an earlier call leaks into a later one
+    for i, (B, layers, E, S, kmax) in enumerate([(300, 2, 64, 16, 15), (40, 4, 1024, 16, 15),
+                                                 (7, 1, 8, 4, 3), (1, 1, 8, 4, 0),
+                                                 (300, 3, 16, 8, 32)]):
+        code, st = run_both(*case(1000 + i, B, layers, E, S, kmax))
+        assert code == 0 and (st == 0).all(), (B, code)
