@@ -448,14 +448,35 @@ __global__ void __launch_bounds__(kRowpassThreads, kRowpassCtasPerSm) rowpass_ke
             nan_seen |= vm != vm;
             if (vm > m) raise(vm);
             if (m != -INFINITY) {
-              float e[2 * EPV];
+              if constexpr (BF16) {
+                // element pairs: one f32x2 FMA for two shifts, the 16 terms
+                // summed as eight pairs by a tree of f32x2 adds, then the
+                // pair's halves
+                const uint64_t c2p = pk2(c2, c2), nmp = pk2(-mc2, -mc2);
+                uint64_t r[EPV];
 #pragma unroll
-              for (int k = 0; k < 2 * EPV; ++k) e[k] = term(x[k]);
+                for (int k = 0; k < EPV; ++k) {
+                  float a0, a1;
+                  upk2(fma2(pk2(x[2 * k], x[2 * k + 1]), c2p, nmp), a0, a1);
+                  r[k] = pk2(ex2_approx(a0), ex2_approx(a1));
+                }
 #pragma unroll
-              for (int w2 = 1; w2 < 2 * EPV; w2 <<= 1)
+                for (int w2 = 1; w2 < EPV; w2 <<= 1)
 #pragma unroll
-                for (int k = 0; k + w2 < 2 * EPV; k += 2 * w2) e[k] += e[k + w2];
-              add(e[0]);
+                  for (int k = 0; k + w2 < EPV; k += 2 * w2) r[k] = add2(r[k], r[k + w2]);
+                float lo2, hi2;
+                upk2(r[0], lo2, hi2);
+                add(lo2 + hi2);
+              } else {
+                float e[2 * EPV];
+#pragma unroll
+                for (int k = 0; k < 2 * EPV; ++k) e[k] = term(x[k]);
+#pragma unroll
+                for (int w2 = 1; w2 < 2 * EPV; w2 <<= 1)
+#pragma unroll
+                  for (int k = 0; k + w2 < 2 * EPV; k += 2 * w2) e[k] += e[k + w2];
+                add(e[0]);
+              }
             }
           }
         } else {
