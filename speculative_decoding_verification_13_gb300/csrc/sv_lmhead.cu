@@ -8,8 +8,9 @@
 // Computing them in the epilogue means the logits never reach memory.
 //
 // Persistent CTAs (one per SM), work units of one 128-row tile of H by
-// kNChunk 256-column tiles of W.  Warp 0: TMA producer (one lane) filling a
-// 4-stage ring of 128-byte-swizzled 128x64 (H) and 256x64 (W) bf16 tiles.
+// nchunk 256-column tiles of W (32, 16 or 8, chosen per call).  Warp 0: TMA
+// producer (one lane) filling a 4-stage ring of 128-byte-swizzled 128x64 (H)
+// and 256x64 (W) bf16 tiles.
 // Warp 1: TMEM allocation and the MMA issuer (one lane): 128x256x16
 // tcgen05.mma (kind::f16, bf16 inputs, f32 accumulators in TMEM), four per
 // 64-wide K block, into one of two 256-column accumulators.  Warps 2-5: the
@@ -30,7 +31,7 @@ constexpr int kLmThreads = 192;                       // 6 warps
 constexpr int kTileA = BM * BK * 2;                   // 16 KB
 constexpr int kTileB = BN * BK * 2;                   // 32 KB
 constexpr int kLmStageBytes = kTileA + kTileB;        // 48 KB
-constexpr int kNChunk = 8;                            // W tiles per work unit
+constexpr int kNChunkMin = 8;                         // fewest W tiles per work unit
 constexpr uint32_t kTmemCols = 2 * BN;                // two accumulators
 constexpr size_t kLmSmem = size_t(kLmStages) * kLmStageBytes + 1024;  // + alignment slack
 
@@ -42,6 +43,7 @@ struct LmPartial {
 struct LmArgs {
   int M, V, K;
   int mtiles, ntiles, n_chunks, kblocks;
+  int nchunk;                // W tiles per work unit
   const float* temperature;  // [M]
   const int32_t* tokens;     // [M] or null
   LmPartial* part;           // [n_chunks, M]
@@ -153,8 +155,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     bool stop = false;
     for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
       const int mt = u % A.mtiles, c = u / A.mtiles;
-      const int nt1 = min((c + 1) * kNChunk, A.ntiles);
-      for (int nt = c * kNChunk; nt < nt1 && !stop; ++nt)
+      const int nt1 = min((c + 1) * A.nchunk, A.ntiles);
+      for (int nt = c * A.nchunk; nt < nt1 && !stop; ++nt)
         for (int kb = 0; kb < A.kblocks; ++kb) {
           if (!lm_wait(empty0 + 8u * stage, phase ^ 1u, &abort_flag, 32)) {
             stop = true;
@@ -187,8 +189,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     long long commits = 0;  // accumulator commits issued
     for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x) {
       const int c = u / A.mtiles;
-      const int nt1 = min((c + 1) * kNChunk, A.ntiles);
-      for (int nt = c * kNChunk; nt < nt1 && !stop; ++nt) {
+      const int nt1 = min((c + 1) * A.nchunk, A.ntiles);
+      for (int nt = c * A.nchunk; nt < nt1 && !stop; ++nt) {
         if (!lm_wait(aempty0 + 8u * ab, aphase ^ 1u, &abort_flag, 64)) {
           stop = true;
           break;
@@ -240,8 +242,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const int tok = live && A.tokens ? A.tokens[row] : -1;
       float best = -INFINITY, s = 0.f, xt = __int_as_float(0x7fc00000);
       int arg = -1;
-      const int nt1 = min((c + 1) * kNChunk, A.ntiles);
-      for (int nt = c * kNChunk; nt < nt1; ++nt) {
+      const int nt1 = min((c + 1) * A.nchunk, A.ntiles);
+      for (int nt = c * A.nchunk; nt < nt1; ++nt) {
         if (!lm_wait(afull0 + 8u * ab, aphase, &abort_flag, 128)) {
           stop = true;
           break;
@@ -356,11 +358,32 @@ bool make_map(CUtensorMap* map, const void* data, int rows, int K, int box_rows)
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W tiles per work unit: of 32, 16 and 8, the one that leaves the busiest
+// CTA the fewest tiles (units in whole rounds over the grid), the larger on a
+// tie.  Longer runs on one column chunk measured faster: the CTAs that share
+// a W tile (one per row tile) stay on it together (4096 x 151936 x 4096:
+// 32 tiles 2-4 % faster than 8 or 16; 24, which leaves a part-filled last
+// round, 7 % slower).
+int lm_nchunk(int mtiles, int ntiles, int sms) {
+  int best = kNChunkMin;
+  int64_t best_load = INT64_MAX;
+  for (int c = 32; c >= kNChunkMin; c >>= 1) {
+    const int64_t units = int64_t(mtiles) * ((ntiles + c - 1) / c);
+    const int64_t grid = units < sms ? units : sms;
+    const int64_t load = (units + grid - 1) / grid * c;
+    if (load < best_load) {
+      best_load = load;
+      best = c;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 size_t lmhead_workspace_bytes(int M, int V) {
   const int ntiles = (V + BN - 1) / BN;
-  const int n_chunks = (ntiles + kNChunk - 1) / kNChunk;
+  const int n_chunks = (ntiles + kNChunkMin - 1) / kNChunkMin;  // the most chunks a call uses
   return align256(sizeof(WsHeader)) + align256(sizeof(LmPartial) * size_t(n_chunks) * size_t(M > 0 ? M : 1));
 }
 
@@ -383,7 +406,8 @@ int launch_lmhead_stats(const void* H, const void* W, int M, int V, int K,
   A.K = K;
   A.mtiles = (M + BM - 1) / BM;
   A.ntiles = (V + BN - 1) / BN;
-  A.n_chunks = (A.ntiles + kNChunk - 1) / kNChunk;
+  A.nchunk = lm_nchunk(A.mtiles, A.ntiles, sms);
+  A.n_chunks = (A.ntiles + A.nchunk - 1) / A.nchunk;
   A.kblocks = (K + BK - 1) / BK;
   A.temperature = temperature;
   A.tokens = tokens;
