@@ -51,7 +51,9 @@ def run(M, V, d, seed, scale=1.0, greedy_frac=0.25, tokens=True):
     (128, 256, 64),        # one tile, one K block
     (200, 1000, 256),      # ragged row and column tiles
     (130, 3000, 520),      # K not a multiple of the 64-wide K block
-    (256, 151936, 1024),   # the Qwen3 vocabulary, many column chunks
+    (256, 151936, 1024),   # the Qwen3 vocabulary, many column chunks (8 W tiles a unit)
+    (512, 151936, 128),    # 16 W tiles a work unit on a 152-SM GPU
+    (1024, 151936, 128),   # 32 W tiles a work unit on a 152-SM GPU
 ])
 def test_matches_oracle(M, V, d):
     run(M, V, d, seed=M + V + d)
