@@ -38,6 +38,7 @@ METRIC = "spec-verify rows/s and HBM GB/s vs ~8 TB/s peak at B=256,k=15,V=151936
 UNIT = "rows/s"
 EVENT_EVERY = 8  # draft-sampler line: timed steps per row-pass event pair
 ROWPASS_STEPS = 32  # verification line: steps timed for the row passes alone, after the K steps
+INLINE_DRAW_V = 2048  # the library draws final tokens in the deciding warps up to this vocabulary
 L2_BYTES = 129 * 1000 * 1000
 FLUSH_BYTES = 512 << 20  # written between steps when the inputs fit in L2
 
@@ -925,7 +926,10 @@ def main():
                      "bytes_per_launch": bytes_req, "launch_ms": rowpass_ms,
                      "launches_timed": len(timed)},
         "e2e": e2e,
-        "gpu_launches": (6 if top_k is not None else 5) * args.steps,
+        # setup, row pass, [threshold row pass], filter / decide, [draw pass,
+        # locate]: vocabularies up to INLINE_DRAW_V take their draws in the
+        # decide warps, without the last two launches
+        "gpu_launches": (3 + (top_k is not None) + (2 if V > INLINE_DRAW_V else 0)) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
         "parity": parity,

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libspecverify.so")
 SOURCES = ["sv_api.cu", "sv_setup.cu", "sv_rowpass.cu", "sv_finalize.cu", "sv_draw.cu", "sv_noalloc.cu", "sv_kv.cu", "sv_lmhead.cu", "sv_adapt.cu", "sv_greedy.cu"]
-HEADERS = ["sv_internal.cuh", "sv_select.cuh", "sv_bigrow.cuh"]
+HEADERS = ["sv_internal.cuh", "sv_select.cuh", "sv_bigrow.cuh", "sv_weights.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr"]

@@ -115,7 +115,7 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   if (int rc = prepare_device(t.vocab, &ds)) return rc;
   const int sms = ds.sms;
 
-  Problem P;
+  Problem P{};
   P.target = t.data;
   P.draft = d.data;
   P.t_stride = t.row_stride;
@@ -136,6 +136,7 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   P.out_q = nullptr;
   P.n_seg = 1;
   P.test_expire = options ? options->test_expire_wait : 0;
+  P.inline_draw = t.vocab <= kInlineDrawV;
   P.ws = ws_bind(workspace, L);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -163,6 +164,8 @@ int spec_verify(const sv_logits* target_logits, const sv_logits* draft_logits,
   const int64_t fmax = int64_t(sms) * ds.occ_filter;
   if (launch_filter_decide(P, bf16, int(fjobs < fmax ? fjobs : fmax), s) != cudaSuccess)
     return SV_ERR_CUDA;
+  // short rows: every draw was taken by its decide job
+  if (P.inline_draw) return SV_OK;
   // draw pass: a queued draw is cut into segments so that the units (draws x
   // segments) outnumber the resident CTAs about kDrawUnitsPerCta-fold and the
   // last round is short (at most one queued draw per request); then the
@@ -208,7 +211,7 @@ int spec_draft_sample(const sv_logits* draft_logits, const int32_t* k_per_req,
   if (int rc = prepare_device(x.vocab, &ds)) return rc;
   const int sms = ds.sms;
 
-  Problem P;
+  Problem P{};
   P.target = x.data;
   P.draft = nullptr;
   P.t_stride = x.row_stride;

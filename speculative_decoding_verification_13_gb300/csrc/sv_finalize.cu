@@ -20,10 +20,12 @@
 //                 "Speculative decoding…", "Draft and verify", step Three).
 //                 Unfiltered sampling: accept while u_i < p_i(x_i) / q_i(x_i),
 //                 stop at the first rejection, then queue the final draw for
-//                 the draw pass.
+//                 the draw pass (vocabularies up to kInlineDrawV: draw it in
+//                 the warp, and the draw pass is not launched).
 #include <math.h>
 
 #include "sv_select.cuh"
+#include "sv_weights.cuh"
 
 namespace sv {
 namespace {
@@ -698,7 +700,80 @@ __device__ void fail_request(const Problem& P, int b, int k, int t0, int d0) {
   if (lane == 0) P.out_accept_len[b] = -1;
 }
 
+// The final token of a sampled decide job drawn in the deciding warp, for
+// rows of at most kInlineDrawV elements: y* = min{ y : C_y > t }, t = floor(u S),
+// over the weights of the draw pass (residual max(0, p_L - q_L), or p_k; kept-
+// set masks of threshold rows; the residual falls back to p_L if its mass
+// vanished through rounding), each as an exact 2^-40 fixed-point integer.
+// Lane l takes a contiguous run of elements (a multiple of 8 long): one pass
+// forms the lane sums, their scan gives S and each lane's first prefix, and
+// the lane holding t walks its run again.  Short loops, not unrolled: this
+// warp's code runs once per request, so its footprint sets its speed.
+// -1 if the row has no mass.
+template <bool BF16>
+__device__ __noinline__ int draw_in_warp(const Problem& P, const DrawDesc& d) {
+  using E = Elt<BF16>;
+  const int lane = threadIdx.x & 31;
+  Weights W = make_weights(d);
+  const unsigned char* trow =
+      static_cast<const unsigned char*>(P.target) + d.tr * P.t_stride * E::kSize;
+  const unsigned char* drow =
+      d.kind == 1 ? static_cast<const unsigned char*>(P.draft) + (d.dr - P.Rt) * P.d_stride * E::kSize
+                  : nullptr;
+  const int V = P.V, fast_end = V & ~7;
+  const int run = ((V + 255) / 256) * 8;  // elements per lane, a multiple of 8
+  const int e0 = lane * run, e1 = min(e0 + run, V);
+  // fixed-point weights of elements e .. e + 7 (16-byte loads where all 8 lie
+  // below fast_end; rows start 16-byte aligned)
+  auto weights8 = [&](int e, unsigned long long* wf) {
+    float xt[8], xd[8];
+    elems8<BF16>(trow + size_t(e) * E::kSize, trow, e, fast_end, V, xt);
+    if (W.kind == 1) elems8<BF16>(drow + size_t(e) * E::kSize, drow, e, fast_end, V, xd);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wf[k] = fixw(W.at(xt[k], W.kind == 1 ? xd[k] : 0.f, e + k));
+  };
+  auto lane_sum = [&]() {
+    unsigned long long ls = 0ull, wf[8];
+#pragma unroll 1
+    for (int e = e0; e < e1; e += 8) {
+      weights8(e, wf);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls += wf[k];
+    }
+    return ls;
+  };
+  unsigned long long ls = lane_sum();
+  unsigned long long S = warp_sum_u64(ls);
+  if (W.kind == 1 && S == 0ull) {
+    W.set_kind(2);
+    ls = lane_sum();
+    S = warp_sum_u64(ls);
+  }
+  if (S == 0ull) return -1;
+  const unsigned long long ufix = (unsigned long long)(d.u * 4294967296.0);  // exact
+  const unsigned long long t = (__umul64hi(S, ufix) << 32) | ((S * ufix) >> 32);
+  // the lane whose run holds the first prefix above t (t < S), then the element
+  const unsigned long long incl = warp_incl_scan_u64(ls);
+  const uint32_t hit = __ballot_sync(kFull, ls > 0ull && incl > t);
+  const int owner = __ffs(hit) - 1;
+  int y = -1;
+  if (lane == owner) {
+    unsigned long long pre = incl - ls, wf[8];
+#pragma unroll 1
+    for (int e = e0; e < e1 && y < 0; e += 8) {
+      weights8(e, wf);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        pre += wf[k];
+        if (y < 0 && wf[k] > 0ull && pre > t) y = e + k;
+      }
+    }
+  }
+  return __shfl_sync(kFull, y, owner);
+}
+
 // Decide job of a request that is not filtered (or has a data error).
+template <bool BF16>
 __device__ __noinline__ void decide_request(const Problem& P, int b) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
@@ -711,11 +786,11 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
   const float T = P.temperature[b];
   const bool greedy = T == 0.0f;
   const int L = decide(P, b, k, t0, d0, greedy);
-  if (lane != 0) return;
   if (greedy) {
-    P.out_tokens[t0 + L] = w.stats[t0 + L].arg;
+    if (lane == 0) P.out_tokens[t0 + L] = w.stats[t0 + L].arg;
     return;
   }
+  if (lane != 0 && !P.inline_draw) return;
   DrawDesc d;
   const RowStat st = w.stats[t0 + L];
   d.tr = t0 + L;
@@ -738,6 +813,15 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
   d.u = double(P.uniforms[t0 + k]);
   d.t0 = t0;
   d.L = L;
+  if (P.inline_draw) {
+    // every lane formed the same descriptor
+    const int y = draw_in_warp<BF16>(P, d);
+    if (lane == 0) {
+      if (y < 0) record_error(w.hdr, SV_ERR_INTERNAL, -1, d.tr);  // no mass found
+      P.out_tokens[t0 + L] = y;
+    }
+    return;
+  }
   w.draw[atomicAdd(&w.hdr->n_draw, 1)] = d;
 }
 
@@ -1133,7 +1217,7 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
       __syncthreads();  // the scratch is reused by the next unit
     } else {
       const int j = (u - nf) * kWarps + warp;
-      if (j < nd) decide_request(P, w.job[P.B + j].x);
+      if (j < nd) decide_request<BF16>(P, w.job[P.B + j].x);
     }
   }
 }

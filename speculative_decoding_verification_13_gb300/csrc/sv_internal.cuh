@@ -29,6 +29,10 @@ constexpr uint32_t kWaitPolls = 1u << 28;                // ... or after this ma
 constexpr uint64_t kTestWaitNs = 1000ull * 1000;         // the expiring test wait: 1 ms
 constexpr int kMaxSeg = 16;                              // draw-pass segments per row (at most)
 constexpr int kDrawUnitsPerCta = 8;                      // draw-pass units per resident CTA (target)
+// Vocabularies up to this size draw the final token of a decide job in the
+// deciding warp: a pass for S and one for the crossing over a few tiles cost
+// less than the two dependent launches of the draw pass and the locate kernel.
+constexpr int kInlineDrawV = 2048;
 
 // Row modes chosen per request by the setup kernel.  kTopk: a filtered row
 // whose top-k is active and at most SV_TOPK_MAX (candidates captured in one
@@ -175,6 +179,8 @@ struct Problem {
   int32_t B;
   int32_t n_seg;                // draw-pass segments per queued draw (1..kMaxSeg)
   int32_t test_expire;          // test only: one bounded wait of the row pass expires
+  int32_t inline_draw;          // rows of at most kInlineDrawV elements: decide jobs draw
+                                // their final token in place (no draw pass, no locate)
   const int32_t* draft_tokens;
   const int32_t* k_per_req;
   const float* temperature;

@@ -183,6 +183,19 @@ def test_vocab_sizes_and_ragged_tails(V, dtype):
               f"V={V} filtered")
 
 
+@pytest.mark.parametrize("V", [2048, 2049])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_draws_either_side_of_the_in_warp_draw(V, dtype):
+    # up to 2048 elements the deciding warp takes the final draw itself; from
+    # 2049 the draw pass and the locate kernel do: residuals and bonus draws,
+    # unfiltered and by a kept-set threshold (top-p alone), on both sides
+    k = [0, 1, 3, 5, 2, 7, 4, 6]
+    T = [1.0, 0.0, 0.9, 1.3, 0.6, 1.0, 2.0, 0.8]
+    check(custom(k, T, V, dtype, sig=0.5, seed=V), f"V={V}")
+    check(custom(k, T, V, dtype, top_p=[0.9, 1.0, 0.5, 0.95, 0.3, 0.99, 0.9, 0.7], sig=0.5,
+                 seed=V + 1), f"V={V} top-p alone")
+
+
 def test_unaligned_row_stride_is_rejected_on_the_host():
     b = W.make_batch_from_params("edge", [1], [1.0], [1.0], 3, torch.float32, 5, device=DEV)
     with pytest.raises(sv.SpecVerifyError, match="UNSUPPORTED"):
