@@ -773,7 +773,11 @@ __device__ __noinline__ int draw_in_warp(const Problem& P, const DrawDesc& d) {
 }
 
 // Decide job of a request that is not filtered (or has a data error).
-template <bool BF16>
+// INLINE: the sampled requests' final draws are taken here (draw_in_warp);
+// otherwise they are queued for the draw pass.  The two are separate kernel
+// instances: the in-warp draw's code in the kernel of the long-row workloads
+// measured 2-4 µs on their filter / decide kernel (instruction fetch).
+template <bool BF16, bool INLINE>
 __device__ __noinline__ void decide_request(const Problem& P, int b) {
   const Ws& w = P.ws;
   const int lane = threadIdx.x & 31;
@@ -786,11 +790,11 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
   const float T = P.temperature[b];
   const bool greedy = T == 0.0f;
   const int L = decide(P, b, k, t0, d0, greedy);
+  if (!INLINE && lane != 0) return;
   if (greedy) {
     if (lane == 0) P.out_tokens[t0 + L] = w.stats[t0 + L].arg;
     return;
   }
-  if (lane != 0 && !P.inline_draw) return;
   DrawDesc d;
   const RowStat st = w.stats[t0 + L];
   d.tr = t0 + L;
@@ -813,16 +817,16 @@ __device__ __noinline__ void decide_request(const Problem& P, int b) {
   d.u = double(P.uniforms[t0 + k]);
   d.t0 = t0;
   d.L = L;
-  if (P.inline_draw) {
+  if constexpr (INLINE) {
     // every lane formed the same descriptor
     const int y = draw_in_warp<BF16>(P, d);
     if (lane == 0) {
       if (y < 0) record_error(w.hdr, SV_ERR_INTERNAL, -1, d.tr);  // no mass found
       P.out_tokens[t0 + L] = y;
     }
-    return;
+  } else {
+    w.draw[atomicAdd(&w.hdr->n_draw, 1)] = d;
   }
-  w.draw[atomicAdd(&w.hdr->n_draw, 1)] = d;
 }
 
 // Final draw of a filtered request from the kept sets, by inverse CDF in
@@ -1174,7 +1178,7 @@ __device__ void filtered_request(const Problem& P, int b, int t0, int k, const R
 
 // Persistent CTAs over the job lists: a filtered request takes a whole CTA;
 // the other requests are decided kWarps at a time, one warp each.
-template <bool BF16>
+template <bool BF16, bool INLINE>
 __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Problem P) {
   extern __shared__ __align__(16) unsigned char post_smem[];
   WarpScratch* scr = reinterpret_cast<WarpScratch*>(post_smem);
@@ -1217,7 +1221,7 @@ __global__ void __launch_bounds__(kPostThreads, 2) filter_decide_kernel(const Pr
       __syncthreads();  // the scratch is reused by the next unit
     } else {
       const int j = (u - nf) * kWarps + warp;
-      if (j < nd) decide_request<BF16>(P, w.job[P.B + j].x);
+      if (j < nd) decide_request<BF16, INLINE>(P, w.job[P.B + j].x);
     }
   }
 }
@@ -1323,19 +1327,27 @@ size_t filter_smem_bytes() { return sizeof(WarpScratch) * kWarps; }
 
 cudaError_t launch_filter_decide(const Problem& P, bool bf16, int grid, cudaStream_t s) {
   const size_t smem = filter_smem_bytes();
-  if (bf16)
-    return launch_after(filter_decide_kernel<true>, grid, kPostThreads, smem, s, P);
-  return launch_after(filter_decide_kernel<false>, grid, kPostThreads, smem, s, P);
+  if (P.inline_draw)
+    return bf16 ? launch_after(filter_decide_kernel<true, true>, grid, kPostThreads, smem, s, P)
+                : launch_after(filter_decide_kernel<false, true>, grid, kPostThreads, smem, s, P);
+  return bf16 ? launch_after(filter_decide_kernel<true, false>, grid, kPostThreads, smem, s, P)
+              : launch_after(filter_decide_kernel<false, false>, grid, kPostThreads, smem, s, P);
 }
 
 // Shared-memory limit and resident CTAs per SM of the filter / decide kernel
 // (host queries; nothing is allocated).
 cudaError_t filter_occupancy(int* occ) {
   const int smem = int(filter_smem_bytes());
-  cudaError_t e = cudaFuncSetAttribute(filter_decide_kernel<true>,
+  cudaError_t e = cudaFuncSetAttribute(filter_decide_kernel<true, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(filter_decide_kernel<false>,
+    e = cudaFuncSetAttribute(filter_decide_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(filter_decide_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(filter_decide_kernel<false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sample_post_kernel<true>,
@@ -1343,15 +1355,21 @@ cudaError_t filter_occupancy(int* occ) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(sample_post_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0, d = 0;
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, filter_decide_kernel<true>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, filter_decide_kernel<true, false>,
                                                       kPostThreads, smem);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, filter_decide_kernel<false>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, filter_decide_kernel<false, false>,
+                                                      kPostThreads, smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, filter_decide_kernel<true, true>,
+                                                      kPostThreads, smem);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, filter_decide_kernel<false, true>,
                                                       kPostThreads, smem);
   if (e != cudaSuccess) return e;
-  *occ = max(1, min(a, b));
+  *occ = max(1, min(min(a, b), min(c, d)));
   return cudaSuccess;
 }
 
